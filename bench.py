@@ -1,0 +1,492 @@
+#!/usr/bin/env python3
+"""Benchmark of the HCCL-style collective data plane on one GB300.
+
+Default workload (one "step" = one AllReduce call over the whole batch):
+  Ring AllReduce, sum, P = 8 virtual ranks, fp32, 16,777,216 elements per rank
+  (64 MiB per rank), values N(0,1) * 1e-3 (synthetic gradients, seed 0),
+  fused mode (one kernel per call), out of place.
+Metric: effective algbw = n * b / t (bytes of one rank's vector per second of
+one call), GB/s.  The inputs (512 MiB) and outputs (512 MiB) are larger than
+the 129 MB L2, so no flush is needed between calls.
+
+Prints one JSON line (rank 0).  Other workloads (--workload) print the same
+line for the other configurations.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import hc_inputs  # noqa: E402
+
+METRIC = "AllReduce effective algbw GB/s and % of HBM roofline vs P, size, algo (1xGB300)"
+
+WORKLOADS = {
+    "ring_fp32_p8": dict(desc="Ring AllReduce sum, P=8 virtual ranks, fp32, 16,777,216 elements "
+                              "per rank (64 MiB), N(0,1)*1e-3, fused mode, out of place",
+                         algo="ring", coll="allreduce", P=8, n=16777216, dtype="float32", op="sum",
+                         mode="fused", p_intra=1, loop_bytes=0, scale=1e-3),
+    "ring_fp32_p8_step": dict(desc="Ring AllReduce sum, P=8, fp32, 16,777,216 elements per rank, "
+                                   "step-faithful mode (14 launches)",
+                              algo="ring", coll="allreduce", P=8, n=16777216, dtype="float32",
+                              op="sum", mode="step", p_intra=1, loop_bytes=0, scale=1e-3),
+    "ring_fp32_p8_rs": dict(desc="Ring ReduceScatter sum, P=8, fp32, 16,777,216 elements per rank, fused",
+                            algo="ring", coll="reducescatter", P=8, n=16777216, dtype="float32",
+                            op="sum", mode="fused", p_intra=1, loop_bytes=0, scale=1e-3),
+    "ring_fp32_p8_ag": dict(desc="Ring AllGather, P=8, fp32, 16,777,216 elements per rank, fused, "
+                                 "out of place",
+                            algo="ring", coll="allgather", P=8, n=16777216, dtype="float32",
+                            op="sum", mode="fused", p_intra=1, loop_bytes=0, scale=1e-3),
+    "ring_bf16_p8": dict(desc="Ring AllReduce sum, P=8, bf16 (per-step rounding), 67,108,864 "
+                              "elements per rank (128 MiB), N(0,1)*1e-2, fused",
+                         algo="ring", coll="allreduce", P=8, n=67108864, dtype="bfloat16", op="sum",
+                         mode="fused", p_intra=1, loop_bytes=0, scale=1e-2),
+    "rhd_bf16_p8": dict(desc="RHD AllReduce sum, P=8, bf16, 67,108,864 elements per rank, fused",
+                        algo="rhd", coll="allreduce", P=8, n=67108864, dtype="bfloat16", op="sum",
+                        mode="fused", p_intra=1, loop_bytes=0, scale=1e-2),
+    "rhd_bf16_p8_max": dict(desc="RHD AllReduce max, P=8, bf16, 67,108,864 elements per rank, fused",
+                            algo="rhd", coll="allreduce", P=8, n=67108864, dtype="bfloat16",
+                            op="max", mode="fused", p_intra=1, loop_bytes=0, scale=1e-2),
+    "pipe_fp32_4x8": dict(desc="Pipeline AllReduce sum, 4 servers x 8 ranks (P=32), fp32, "
+                               "8,388,608 elements per rank (32 MiB), N(0,1)*1e-3, fused",
+                          algo="pipeline", coll="allreduce", P=32, n=8388608, dtype="float32",
+                          op="sum", mode="fused", p_intra=8, loop_bytes=0, scale=1e-3),
+    "pipe_fp32_4x8_step": dict(desc="Pipeline AllReduce sum, 4x8, fp32, 8,388,608 elements per "
+                                    "rank, step mode, 64 MiB loop limit (4 loops, tail 37,504)",
+                               algo="pipeline", coll="allreduce", P=32, n=8388608,
+                               dtype="float32", op="sum", mode="step", p_intra=8,
+                               loop_bytes=64 << 20, scale=1e-3),
+    "rhd_fp32_p8_small": dict(desc="RHD AllReduce sum, P=8, fp32, 4096 elements per rank "
+                                   "(latency regime, L2-resident), fused",
+                              algo="rhd", coll="allreduce", P=8, n=4096, dtype="float32",
+                              op="sum", mode="fused", p_intra=1, loop_bytes=0, scale=1.0),
+    "rhd_fp32_p8_small_step": dict(desc="RHD AllReduce sum, P=8, fp32, 4096 elements per rank, "
+                                        "step mode (6 launches)",
+                                   algo="rhd", coll="allreduce", P=8, n=4096, dtype="float32",
+                                   op="sum", mode="step", p_intra=1, loop_bytes=0, scale=1.0),
+}
+DTYPE_TAG = {"float32": "f32", "bfloat16": "bf16", "int32": "int32"}
+ESIZE = {"float32": 4, "bfloat16": 2, "int32": 4}
+KERNEL_FILE = os.path.join(ROOT, "collective_communication_algorithms_gb300", "csrc",
+                           "hc_kernels.cu")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="ring_fp32_p8", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def algorithmic_bytes(w):
+    """Minimum bytes one fused call moves (reads + writes)."""
+    P, n, b = w["P"], w["n"], ESIZE[w["dtype"]]
+    if w["coll"] == "allreduce":
+        return 2 * P * n * b
+    if w["coll"] == "reducescatter":
+        return (P + 1) * n * b
+    return (P + 1) * n * b  # allgather out of place
+
+
+def inputs_for(w, n=None):
+    n = w["n"] if n is None else n
+    if w["dtype"] == "float32":
+        return hc_inputs.gradients_f32(w["P"], n, seed=0, scale=w["scale"])
+    if w["dtype"] == "bfloat16":
+        return hc_inputs.gradients_bf16(w["P"], n, seed=0, scale=w["scale"])
+    return hc_inputs.uniform_int32(w["P"], n, seed=0)
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    with open(KERNEL_FILE, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def traffic_from_profiles(workload):
+    """dram read+write bytes per launch of the dominant kernel from a
+    committed ncu summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        e = t.get(workload)
+        if e and e.get("kernel_source_sha256_16") == kernel_source_hash():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled with nvidia-smi while the GPU runs the step
+# ---------------------------------------------------------------------------
+CLOCK_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, device_uuid):
+        self.proc = None
+        self.out = os.path.join("/tmp", "hc_bench_clocks_%d.csv" % os.getpid())
+        cmd = ["nvidia-smi", "--query-gpu=" + CLOCK_FIELDS, "--format=csv,noheader,nounits",
+               "-lms", "100"]
+        if device_uuid:
+            cmd += ["-i", device_uuid]
+        try:
+            self.f = open(self.out, "w")
+            self.proc = subprocess.Popen(cmd, stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"error": "nvidia-smi unavailable"}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.out) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    mx.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for name, v in zip(names, parts[4:8]):
+                    if v.lower().startswith("active"):
+                        reasons.add(name)
+        os.remove(self.out)
+        if not sm:
+            return {"error": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# our implementation
+# ---------------------------------------------------------------------------
+def run_ours(args, w):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    from collective_communication_algorithms_gb300 import _binding as B
+    B.lib()  # loud failure if the library is missing
+
+    P, n, dt = w["P"], w["n"], w["dtype"]
+    b = ESIZE[dt]
+    tdt = {"float32": torch.float32, "bfloat16": torch.int16, "int32": torch.int32}[dt]
+    X = inputs_for(w)
+    Xt = torch.from_numpy(X.view(np.int16) if dt == "bfloat16" else X)
+    send = Xt.to(dev)
+    recv = torch.empty_like(send)
+    send_p = [send[r].data_ptr() for r in range(P)]
+    recv_p = [recv[r].data_ptr() for r in range(P)]
+    if w["coll"] == "reducescatter":
+        segs = [B.hc_segment_range(w["algo"], w["coll"], P, n, dt, k) for k in range(P)]
+        rs_out = [torch.empty(max(ln, 8), dtype=tdt, device=dev) for _, ln in segs]
+        recv_p = [t.data_ptr() for t in rs_out]
+    if w["coll"] == "allgather":
+        segs = [B.hc_segment_range(w["algo"], w["coll"], P, n, dt, k) for k in range(P)]
+        ag_in = [send[k, off:off + ln].clone() for k, (off, ln) in enumerate(segs)]
+        send_p = [t.data_ptr() for t in ag_in]
+    opts = B.make_opts(w["mode"], ranks_per_server=w["p_intra"], max_loop_bytes=w["loop_bytes"])
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    stats, _ = B.hc_schedule_stats(w["algo"], w["coll"], P, n, dt, w["p_intra"], w["loop_bytes"])
+    launches = stats["launches_fused"] if w["mode"] == "fused" else stats["launches_step"]
+
+    def call():
+        if w["coll"] == "allreduce":
+            B.hc_allreduce(send_p, recv_p, P, n, dt, w["op"], w["algo"], opts, sh)
+        elif w["coll"] == "reducescatter":
+            B.hc_reduce_scatter(send_p, recv_p, P, n, dt, w["op"], w["algo"], opts, sh)
+        else:
+            B.hc_allgather(send_p, recv_p, P, n, dt, w["algo"], opts, sh)
+
+    # warm-up, then a sustained run of the same step while clocks are sampled
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    sampler = ClockSampler(uuid)
+    t_end = time.time() + 1.5
+    while time.time() < t_end:
+        for _ in range(20):
+            call()
+        torch.cuda.synchronize()
+
+    # timed region: exactly K steps
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev0.record(stream)
+    for i in range(args.steps):
+        ka[i].record(stream)
+        call()
+        kb[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    total_ms = ev0.elapsed_time(ev1)
+    kern_ms = [a.elapsed_time(bb) for a, bb in zip(ka, kb)]
+    if world > 1:
+        t = torch.tensor([total_ms, statistics.mean(kern_ms)], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, kern_avg = float(t[0]), float(t[1])
+    else:
+        kern_avg = statistics.mean(kern_ms)
+    ms_per_step = total_ms / args.steps
+    value = world * n * b / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the C ABI with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        Xh = Xt.pin_memory()
+        Yh = torch.empty((P, n), dtype=Xt.dtype).pin_memory()
+        if w["coll"] == "allreduce":
+            h2d, d2h = P * n * b, P * n * b
+
+            def e2e_step():
+                send.copy_(Xh, non_blocking=True)
+                call()
+                Yh.copy_(recv, non_blocking=True)
+        elif w["coll"] == "reducescatter":
+            h2d, d2h = P * n * b, n * b
+
+            def e2e_step():
+                send.copy_(Xh, non_blocking=True)
+                call()
+                for r in range(P):
+                    ln = segs[r][1]
+                    Yh[r, :ln].copy_(rs_out[r][:ln], non_blocking=True)
+        else:
+            h2d, d2h = n * b, P * n * b
+
+            def e2e_step():
+                for k, (off, ln) in enumerate(segs):
+                    ag_in[k].copy_(Xh[k, off:off + ln], non_blocking=True)
+                call()
+                Yh.copy_(recv, non_blocking=True)
+        for _ in range(max(2, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = e0.elapsed_time(e1) / args.steps
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t[0])
+        e2e = {"value": round(world * n * b / (e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": round(e_ms, 4)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, budget_s=10.0)
+
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    peak, peak_kind = measured_peak()
+    if w["mode"] == "fused":
+        alg = algorithmic_bytes(w)
+    else:
+        alg = stats["step_bytes"]
+    achieved = alg / (kern_avg * 1e-3) / 1e9
+    traffic = traffic_from_profiles(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": DTYPE_TAG[dt],
+        "data": "synthetic (seeded N(0,1) gradients, numpy PCG64 seed 0)",
+        "config": {"workload": w["desc"], "algo": w["algo"], "collective": w["coll"], "P": P,
+                   "elements_per_rank": n, "mode": w["mode"], "op": w["op"],
+                   "ranks_per_server": w["p_intra"], "max_loop_bytes": w["loop_bytes"],
+                   "l2": "inputs (%d MiB) larger than the 129 MB L2; no flush" % (P * n * b >> 20)
+                   if P * n * b > (129 << 20) else "L2-resident (hot-cache latency regime)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "clock_window": "1.5 s sustained run of the same step + the timed steps"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "peak_kind": peak_kind + " (hbm_gbs, copy burst)",
+                     "algorithmic_bytes_per_launch": alg // max(1, launches) if w["mode"] == "step" else alg,
+                     "kernel_ms": round(kern_avg, 5),
+                     "frac_of_8TBps_nominal": round(achieved / 8000.0, 4)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps * launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# the oracle on the host cores (CPU baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_sample_n(w, n_target):
+    A = 16 // ESIZE[w["dtype"]]
+    S = w["P"]
+    return max(S * A, (n_target // (S * A)) * S * A)
+
+
+def time_oracle_once(w, X):
+    import oracle as O
+    t0 = time.perf_counter()
+    O.replay(w["algo"], w["coll"], X, w["op"], w["dtype"], p_intra=w["p_intra"])
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w, budget_s=10.0):
+    ns = oracle_sample_n(w, 1 << 21)
+    X = inputs_for(w, ns)
+    times = []
+    t_start = time.perf_counter()
+    while time.perf_counter() - t_start < budget_s or len(times) < 2:
+        times.append(time_oracle_once(w, X))
+        if len(times) >= 50:
+            break
+    t = statistics.median(times)
+    return {"value": round(ns * ESIZE[w["dtype"]] / t / 1e9, 5), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": "step-by-step replay of the same schedule on the first %d elements of each "
+                      "of the %d rank vectors, median of %d runs (%.1f s), single thread"
+                      % (ns, w["P"], len(times), sum(times)),
+            "cpu": cpu_model()}
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip() + ", %d cores" % os.cpu_count()
+    except Exception:
+        pass
+    return "%d cores" % os.cpu_count()
+
+
+def run_reference(args, w):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    ns = oracle_sample_n(w, 1 << 20)
+    X = inputs_for(w, ns)
+    for _ in range(args.warmup):
+        time_oracle_once(w, X)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        time_oracle_once(w, X)
+    total = time.perf_counter() - t0
+    ms = total / args.steps * 1e3
+    value = ns * ESIZE[w["dtype"]] / (ms * 1e-3) / 1e9
+    sample = ("oracle step-by-step replay (plain C, one thread) of the same schedule on the "
+              "first %d elements of each of the %d rank vectors per step" % (ns, w["P"]))
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 5),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": DTYPE_TAG[w["dtype"]],
+        "data": "synthetic (seeded N(0,1) gradients, numpy PCG64 seed 0)",
+        "config": {"workload": w["desc"], "algo": w["algo"], "collective": w["coll"],
+                   "P": w["P"], "elements_per_rank": w["n"], "mode": "oracle",
+                   "sample_elements_per_rank": ns},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": sample, "cpu": cpu_model()},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_ours(args, w)
+
+
+if __name__ == "__main__":
+    main()

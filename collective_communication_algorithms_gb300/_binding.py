@@ -1,0 +1,215 @@
+"""ctypes binding of libhc (include/hc.h).  Argument marshalling only: every
+step of every collective runs in libhc's CUDA kernels.
+
+The functions named hc_* take raw values exactly like the C entry points
+(device pointers as ints, a stream handle as an int) and raise HcError on a
+non-zero status.  There is no fallback: if libhc.so was not built, loading it
+raises.
+"""
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_lib", "libhc.so")
+MAX_RANKS = 64
+
+DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2}
+OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
+ALGOS = {"ring": 0, "rhd": 1, "pipeline": 2}
+COLLS = {"allreduce": 0, "reducescatter": 1, "allgather": 2}
+MODES = {"fused": 0, "step": 1}
+STATUS = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_UNSUPPORTED", 3: "HC_ERR_ALIGN",
+          4: "HC_ERR_SCRATCH", 5: "HC_ERR_CUDA", 6: "HC_ERR_TIMEOUT"}
+
+
+class HcError(RuntimeError):
+    def __init__(self, status, where):
+        self.status = status
+        self.name = STATUS.get(status, str(status))
+        super().__init__("%s: %s (%s)" % (where, self.name, status_string(status)))
+
+
+class hc_opts_t(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_size_t), ("mode", ctypes.c_int),
+                ("ranks_per_server", ctypes.c_int), ("max_loop_bytes", ctypes.c_size_t),
+                ("scratch", ctypes.c_void_p), ("scratch_bytes", ctypes.c_size_t)]
+
+
+class hc_stats_t(ctypes.Structure):
+    _fields_ = [("struct_size", ctypes.c_size_t), ("steps_per_loop", ctypes.c_int),
+                ("loops", ctypes.c_int), ("chunk", ctypes.c_size_t), ("tail", ctypes.c_size_t),
+                ("launches_step", ctypes.c_int), ("launches_fused", ctypes.c_int),
+                ("step_bytes", ctypes.c_ulonglong), ("fused_bytes", ctypes.c_ulonglong)]
+
+
+class hc_plan_record_t(ctypes.Structure):
+    _fields_ = [("launch", ctypes.c_int32), ("seg", ctypes.c_int32),
+                ("lo", ctypes.c_int64), ("hi", ctypes.c_int64),
+                ("acc_rank", ctypes.c_int32), ("acc_loc", ctypes.c_int32),
+                ("in_loc", ctypes.c_int32), ("in_cnt", ctypes.c_int32),
+                ("out_loc", ctypes.c_int32), ("out_cnt", ctypes.c_int32),
+                ("in_ranks", ctypes.c_int32 * MAX_RANKS),
+                ("out_ranks", ctypes.c_int32 * MAX_RANKS)]
+
+
+# every symbol include/hc.h declares
+EXPORTS = ("hc_allreduce", "hc_reduce_scatter", "hc_allgather", "hc_segment_range",
+           "hc_num_segments", "hc_scratch_bytes", "hc_schedule_stats", "hc_step_plan",
+           "hc_status_string", "hc_version")
+
+_lib = None
+
+
+def lib():
+    """Load libhc.so; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libhc.so is not built (%s); run "
+                               "collective_communication_algorithms_gb300.build.build()" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        ptrs = ctypes.POINTER(ctypes.c_void_p)
+        for name in ("hc_allreduce", "hc_reduce_scatter"):
+            f = getattr(L, name)
+            f.argtypes = [ptrs, ptrs, i32, sz, i32, i32, i32, ctypes.POINTER(hc_opts_t), vp]
+            f.restype = i32
+        L.hc_allgather.argtypes = [ptrs, ptrs, i32, sz, i32, i32, ctypes.POINTER(hc_opts_t), vp]
+        L.hc_allgather.restype = i32
+        L.hc_segment_range.argtypes = [i32, i32, i32, sz, i32, i32,
+                                       ctypes.POINTER(sz), ctypes.POINTER(sz)]
+        L.hc_segment_range.restype = i32
+        L.hc_num_segments.argtypes = [i32, i32, i32]
+        L.hc_num_segments.restype = i32
+        L.hc_scratch_bytes.argtypes = [i32, i32, sz, i32]
+        L.hc_scratch_bytes.restype = sz
+        L.hc_schedule_stats.argtypes = [i32, i32, i32, i32, sz, i32, sz,
+                                        ctypes.POINTER(hc_stats_t),
+                                        ctypes.POINTER(ctypes.c_ulonglong)]
+        L.hc_schedule_stats.restype = i32
+        L.hc_step_plan.argtypes = [i32, i32, i32, i32, sz, i32, sz, i32,
+                                   ctypes.POINTER(hc_plan_record_t), sz,
+                                   ctypes.POINTER(sz), ctypes.POINTER(i32)]
+        L.hc_step_plan.restype = i32
+        L.hc_status_string.argtypes = [i32]
+        L.hc_status_string.restype = ctypes.c_char_p
+        L.hc_version.argtypes = []
+        L.hc_version.restype = i32
+        _lib = L
+    return _lib
+
+
+def status_string(status):
+    try:
+        return lib().hc_status_string(int(status)).decode()
+    except Exception:  # library missing: the code alone
+        return STATUS.get(status, "?")
+
+
+def _check(status, where):
+    if status != 0:
+        raise HcError(status, where)
+
+
+def _ptr_array(ptrs):
+    if ptrs is None:
+        return None
+    arr = (ctypes.c_void_p * len(ptrs))()
+    for i, p in enumerate(ptrs):
+        arr[i] = int(p) if p else None
+    return arr
+
+
+def make_opts(mode="fused", ranks_per_server=1, max_loop_bytes=0, scratch=0, scratch_bytes=0):
+    o = hc_opts_t()
+    o.struct_size = ctypes.sizeof(hc_opts_t)
+    o.mode = MODES[mode] if isinstance(mode, str) else int(mode)
+    o.ranks_per_server = int(ranks_per_server)
+    o.max_loop_bytes = int(max_loop_bytes)
+    o.scratch = int(scratch) if scratch else None
+    o.scratch_bytes = int(scratch_bytes)
+    return o
+
+
+def _enum(table, v):
+    return table[v] if isinstance(v, str) else int(v)
+
+
+def hc_allreduce(send, recv, P, count, dtype, op, algo, opts=None, stream=0):
+    st = lib().hc_allreduce(_ptr_array(send), _ptr_array(recv), int(P), int(count),
+                            _enum(DTYPES, dtype), _enum(OPS, op), _enum(ALGOS, algo),
+                            ctypes.byref(opts) if opts is not None else None,
+                            ctypes.c_void_p(int(stream)) if stream else None)
+    _check(st, "hc_allreduce")
+
+
+def hc_reduce_scatter(send, recv, P, count, dtype, op, algo, opts=None, stream=0):
+    st = lib().hc_reduce_scatter(_ptr_array(send), _ptr_array(recv), int(P), int(count),
+                                 _enum(DTYPES, dtype), _enum(OPS, op), _enum(ALGOS, algo),
+                                 ctypes.byref(opts) if opts is not None else None,
+                                 ctypes.c_void_p(int(stream)) if stream else None)
+    _check(st, "hc_reduce_scatter")
+
+
+def hc_allgather(send, recv, P, count, dtype, algo, opts=None, stream=0):
+    st = lib().hc_allgather(_ptr_array(send), _ptr_array(recv), int(P), int(count),
+                            _enum(DTYPES, dtype), _enum(ALGOS, algo),
+                            ctypes.byref(opts) if opts is not None else None,
+                            ctypes.c_void_p(int(stream)) if stream else None)
+    _check(st, "hc_allgather")
+
+
+def hc_segment_range(algo, coll, P, count, dtype, k):
+    off, ln = ctypes.c_size_t(), ctypes.c_size_t()
+    _check(lib().hc_segment_range(_enum(ALGOS, algo), _enum(COLLS, coll), int(P), int(count),
+                                  _enum(DTYPES, dtype), int(k), ctypes.byref(off),
+                                  ctypes.byref(ln)), "hc_segment_range")
+    return off.value, ln.value
+
+
+def hc_num_segments(algo, coll, P):
+    return lib().hc_num_segments(_enum(ALGOS, algo), _enum(COLLS, coll), int(P))
+
+
+def hc_scratch_bytes(algo, P, count, dtype):
+    return lib().hc_scratch_bytes(_enum(ALGOS, algo), int(P), int(count), _enum(DTYPES, dtype))
+
+
+def hc_schedule_stats(algo, coll, P, count, dtype, ranks_per_server=1, max_loop_bytes=0):
+    """Returns (stats dict, per-rank bytes sent list)."""
+    s = hc_stats_t()
+    s.struct_size = ctypes.sizeof(hc_stats_t)
+    sent = (ctypes.c_ulonglong * int(P))()
+    _check(lib().hc_schedule_stats(_enum(ALGOS, algo), _enum(COLLS, coll), int(P),
+                                   int(ranks_per_server), int(count), _enum(DTYPES, dtype),
+                                   int(max_loop_bytes), ctypes.byref(s), sent),
+           "hc_schedule_stats")
+    d = {name: getattr(s, name) for name, _ in hc_stats_t._fields_ if name != "struct_size"}
+    return d, list(sent)
+
+
+def hc_step_plan(algo, coll, P, count, dtype, ranks_per_server=1, max_loop_bytes=0,
+                 in_place=True):
+    """Returns (list of record dicts, number of launches)."""
+    L = lib()
+    n = ctypes.c_size_t()
+    nl = ctypes.c_int()
+    args = (_enum(ALGOS, algo), _enum(COLLS, coll), int(P), int(ranks_per_server), int(count),
+            _enum(DTYPES, dtype), int(max_loop_bytes), 1 if in_place else 0)
+    _check(L.hc_step_plan(*args, None, 0, ctypes.byref(n), ctypes.byref(nl)), "hc_step_plan")
+    recs = (hc_plan_record_t * max(1, n.value))()
+    _check(L.hc_step_plan(*args, recs, n.value, ctypes.byref(n), ctypes.byref(nl)),
+           "hc_step_plan")
+    out = []
+    for i in range(n.value):
+        r = recs[i]
+        out.append({"launch": r.launch, "seg": r.seg, "lo": r.lo, "hi": r.hi,
+                    "acc_rank": r.acc_rank, "acc_loc": r.acc_loc, "in_loc": r.in_loc,
+                    "out_loc": r.out_loc,
+                    "in_ranks": list(r.in_ranks[:r.in_cnt]),
+                    "out_ranks": list(r.out_ranks[:r.out_cnt])})
+    return out, nl.value
+
+
+def hc_version():
+    return lib().hc_version()

@@ -1,0 +1,388 @@
+// hc_api.cpp -- the C ABI of libhc (see include/hc.h): argument validation,
+// in-place detection, step-plan cache and dispatch to the kernels.
+#include <algorithm>
+#include <cstring>
+#include <map>
+#include <tuple>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "hc_internal.h"
+
+using namespace hc;
+
+namespace {
+
+bool valid_dtype(hc_dtype_t d) { return d == HC_INT32 || d == HC_FLOAT32 || d == HC_BFLOAT16; }
+bool valid_op(hc_op_t o) { return o == HC_SUM || o == HC_PROD || o == HC_MAX || o == HC_MIN; }
+bool valid_algo(hc_algo_t a) { return a == HC_ALGO_RING || a == HC_ALGO_RHD || a == HC_ALGO_PIPELINE; }
+bool valid_coll(hc_coll_t c) {
+    return c == HC_COLL_ALLREDUCE || c == HC_COLL_REDUCE_SCATTER || c == HC_COLL_ALLGATHER;
+}
+
+struct Opts {
+    hc_mode_t mode = HC_MODE_FUSED;
+    int p_intra = 1;
+    int64_t loop_bytes = 0;
+    void* scratch = nullptr;
+    size_t scratch_bytes = 0;
+};
+
+hc_status_t read_opts(const hc_opts_t* o, hc_algo_t algo, int P, Opts* out) {
+    *out = Opts();
+    if (!o) return HC_OK;
+    if (o->struct_size < sizeof(hc_opts_t)) return HC_ERR_INVALID_ARG;
+    if (o->mode != HC_MODE_FUSED && o->mode != HC_MODE_STEP) return HC_ERR_INVALID_ARG;
+    out->mode = o->mode;
+    if (algo == HC_ALGO_PIPELINE) {
+        if (o->ranks_per_server < 1 || P % o->ranks_per_server) return HC_ERR_INVALID_ARG;
+        out->p_intra = o->ranks_per_server;
+    }
+    if (o->max_loop_bytes > (size_t)INT64_MAX) return HC_ERR_INVALID_ARG;
+    out->loop_bytes = (int64_t)o->max_loop_bytes;
+    out->scratch = o->scratch;
+    out->scratch_bytes = o->scratch_bytes;
+    return HC_OK;
+}
+
+struct Interval {
+    uintptr_t lo, hi;
+};
+
+// true when some two intervals overlap (empty intervals ignored)
+bool any_overlap(std::vector<Interval> v) {
+    v.erase(std::remove_if(v.begin(), v.end(), [](const Interval& x) { return x.hi <= x.lo; }),
+            v.end());
+    std::sort(v.begin(), v.end(), [](const Interval& a, const Interval& b) { return a.lo < b.lo; });
+    uintptr_t end = 0;
+    for (size_t i = 0; i < v.size(); i++) {
+        if (i > 0 && v[i].lo < end) return true;
+        end = std::max(end, v[i].hi);
+    }
+    return false;
+}
+
+int sm_count_of_current_device() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev] = v;
+    return v;
+}
+
+// ---------------------------------------------------------------- plan cache
+using PlanKey = std::tuple<int, int, int, int, int64_t, int, int64_t, unsigned long long,
+                           unsigned long long>;
+std::map<PlanKey, Plan>& plan_cache() {
+    static std::map<PlanKey, Plan> m;
+    return m;
+}
+
+const Plan* get_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n,
+                     hc_dtype_t dt, int64_t loop_bytes, const Aliasing& al) {
+    unsigned long long m1 = 0, m2 = 0;
+    for (int r = 0; r < P; r++) {
+        if (al.orig_is_work[r]) m1 |= 1ull << r;
+        if (al.final_is_work[r]) m2 |= 1ull << r;
+    }
+    PlanKey key{(int)algo, (int)coll, P, p_intra, n, (int)dt, loop_bytes, m1, m2};
+    auto& cache = plan_cache();
+    auto it = cache.find(key);
+    if (it != cache.end()) return &it->second;
+    if (cache.size() >= 256) cache.clear();
+    Plan plan;
+    if (!build_plan(algo, coll, P, p_intra, n, dt, loop_bytes, al, &plan)) return nullptr;
+    return &cache.emplace(key, std::move(plan)).first->second;
+}
+
+size_t scratch_stride(size_t n, hc_dtype_t dt) {
+    size_t b = n * (size_t)elem_bytes(dt);
+    return (b + 255) / 256 * 256;
+}
+
+hc_status_t run(hc_coll_t coll, const void* const* send, void* const* recv, int P, size_t count,
+                hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts,
+                cudaStream_t stream) {
+    if (!valid_dtype(dtype) || !valid_op(op) || !valid_algo(algo)) return HC_ERR_INVALID_ARG;
+    if (P < 1 || P > kMaxRanks) return HC_ERR_INVALID_ARG;
+    Opts o;
+    hc_status_t st = read_opts(opts, algo, P, &o);
+    if (st != HC_OK) return st;
+    if (count == 0) return HC_OK;
+    if (count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
+    if (!recv) return HC_ERR_INVALID_ARG;
+    if (!send && coll != HC_COLL_ALLGATHER) return HC_ERR_INVALID_ARG;
+    for (int r = 0; r < P; r++) {
+        if (!recv[r] || (send && !send[r])) return HC_ERR_INVALID_ARG;
+    }
+    for (int r = 0; r < P; r++) {
+        if (((uintptr_t)recv[r] & 15) || (send && ((uintptr_t)send[r] & 15))) return HC_ERR_ALIGN;
+    }
+
+    const int64_t n = (int64_t)count;
+    const int es = elem_bytes(dtype);
+    const Layout lay = make_layout(algo, coll, P, n, dtype);
+    // for ReduceScatter / AllGather, the per-rank segment is the rank's own
+    const Layout own = make_layout(algo, coll, P, n, dtype);
+
+    Aliasing al;
+    std::memset(&al, 0, sizeof al);
+    bool rs_in_place[kMaxRanks] = {false}, ag_in_place[kMaxRanks] = {false};
+    std::vector<Interval> iv;
+    const uintptr_t full = (uintptr_t)n * es;
+    for (int r = 0; r < P; r++) {
+        const uintptr_t d = (uintptr_t)recv[r];
+        if (coll == HC_COLL_ALLREDUCE) {
+            const uintptr_t s = (uintptr_t)send[r];
+            al.orig_is_work[r] = (s == d);
+            al.final_is_work[r] = true;
+            iv.push_back({d, d + full});
+            if (s != d) iv.push_back({s, s + full});
+        } else if (coll == HC_COLL_REDUCE_SCATTER) {
+            const uintptr_t s = (uintptr_t)send[r];
+            const uintptr_t off = (uintptr_t)own.seg_lo(r) * es;
+            const uintptr_t len = (uintptr_t)(own.seg_hi(r) - own.seg_lo(r)) * es;
+            rs_in_place[r] = (d == s + off);
+            iv.push_back({s, s + full});
+            if (!rs_in_place[r]) iv.push_back({d, d + len});
+        } else {
+            const uintptr_t off = (uintptr_t)own.seg_lo(r) * es;
+            const uintptr_t len = (uintptr_t)(own.seg_hi(r) - own.seg_lo(r)) * es;
+            const uintptr_t s = send ? (uintptr_t)send[r] : d + off;
+            ag_in_place[r] = (s == d + off);
+            al.orig_is_work[r] = ag_in_place[r];
+            al.final_is_work[r] = true;
+            iv.push_back({d, d + full});
+            if (!ag_in_place[r]) iv.push_back({s, s + len});
+        }
+    }
+
+    // step-mode ReduceScatter: working memory is the input (in place) or scratch
+    bool need_scratch = false;
+    if (coll == HC_COLL_REDUCE_SCATTER && o.mode == HC_MODE_STEP) {
+        for (int r = 0; r < P; r++) {
+            al.orig_is_work[r] = rs_in_place[r];
+            al.final_is_work[r] = rs_in_place[r];
+            if (!rs_in_place[r]) need_scratch = true;
+        }
+    }
+    if (need_scratch) {
+        const size_t need = (size_t)P * scratch_stride(count, dtype);
+        if (!o.scratch || o.scratch_bytes < need) return HC_ERR_SCRATCH;
+        if ((uintptr_t)o.scratch & 15) return HC_ERR_ALIGN;
+        iv.push_back({(uintptr_t)o.scratch, (uintptr_t)o.scratch + need});
+    }
+    if (any_overlap(iv)) return HC_ERR_INVALID_ARG;
+
+    const int sms = sm_count_of_current_device();
+    if (sms <= 0) return HC_ERR_CUDA;
+
+    if (o.mode == HC_MODE_FUSED) {
+        FusedArgs a;
+        a.algo = algo;
+        a.coll = coll;
+        a.dtype = dtype;
+        a.op = op;
+        a.P = P;
+        a.p_intra = o.p_intra;
+        a.n = n;
+        a.lay = lay;
+        a.send = send;
+        a.recv = recv;
+        std::memcpy(a.ag_in_place, ag_in_place, sizeof ag_in_place);
+        std::memcpy(a.rs_in_place, rs_in_place, sizeof rs_in_place);
+        cudaError_t e = launch_fused(a, stream, sms);
+        return e == cudaSuccess ? HC_OK : HC_ERR_CUDA;
+    }
+
+    const Plan* plan = get_plan(algo, coll, P, o.p_intra, n, dtype, o.loop_bytes, al);
+    if (!plan) return HC_ERR_INVALID_ARG;
+    uintptr_t base[LOC_COUNT][kMaxRanks];
+    std::memset(base, 0, sizeof base);
+    for (int r = 0; r < P; r++) {
+        const uintptr_t d = (uintptr_t)recv[r];
+        if (coll == HC_COLL_ALLREDUCE) {
+            base[LOC_ORIG][r] = (uintptr_t)send[r];
+            base[LOC_WORK][r] = d;
+            base[LOC_FINAL][r] = d;
+        } else if (coll == HC_COLL_REDUCE_SCATTER) {
+            const uintptr_t s = (uintptr_t)send[r];
+            base[LOC_ORIG][r] = s;
+            base[LOC_WORK][r] = rs_in_place[r]
+                                    ? s
+                                    : (uintptr_t)o.scratch + (uintptr_t)r * scratch_stride(count, dtype);
+            base[LOC_FINAL][r] = d - (uintptr_t)own.seg_lo(r) * es;
+        } else {
+            const uintptr_t off = (uintptr_t)own.seg_lo(r) * es;
+            const uintptr_t s = send ? (uintptr_t)send[r] : d + off;
+            base[LOC_ORIG][r] = s - off;
+            base[LOC_WORK][r] = d;
+            base[LOC_FINAL][r] = d;
+        }
+    }
+    cudaError_t e = launch_step(*plan, P, dtype, op, base, stream, sms);
+    return e == cudaSuccess ? HC_OK : HC_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+hc_status_t hc_allreduce(const void* const* send, void* const* recv, int P, size_t count,
+                         hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts,
+                         hc_stream_t stream) {
+    return run(HC_COLL_ALLREDUCE, send, recv, P, count, dtype, op, algo, opts,
+               (cudaStream_t)stream);
+}
+
+hc_status_t hc_reduce_scatter(const void* const* send, void* const* recv, int P, size_t count,
+                              hc_dtype_t dtype, hc_op_t op, hc_algo_t algo,
+                              const hc_opts_t* opts, hc_stream_t stream) {
+    return run(HC_COLL_REDUCE_SCATTER, send, recv, P, count, dtype, op, algo, opts,
+               (cudaStream_t)stream);
+}
+
+hc_status_t hc_allgather(const void* const* send, void* const* recv, int P, size_t count,
+                         hc_dtype_t dtype, hc_algo_t algo, const hc_opts_t* opts,
+                         hc_stream_t stream) {
+    return run(HC_COLL_ALLGATHER, send, recv, P, count, dtype, HC_SUM, algo, opts,
+               (cudaStream_t)stream);
+}
+
+int hc_num_segments(hc_algo_t algo, hc_coll_t coll, int P) {
+    if (!valid_algo(algo) || !valid_coll(coll) || P < 1 || P > kMaxRanks) return 0;
+    return num_segments(algo, coll, P);
+}
+
+hc_status_t hc_segment_range(hc_algo_t algo, hc_coll_t coll, int P, size_t count,
+                             hc_dtype_t dtype, int k, size_t* off, size_t* len) {
+    if (!valid_algo(algo) || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
+    if (P < 1 || P > kMaxRanks || !off || !len) return HC_ERR_INVALID_ARG;
+    if (count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
+    Layout lay = make_layout(algo, coll, P, (int64_t)count, dtype);
+    if (k < 0 || k >= lay.S) return HC_ERR_INVALID_ARG;
+    *off = (size_t)lay.seg_lo(k);
+    *len = (size_t)(lay.seg_hi(k) - lay.seg_lo(k));
+    return HC_OK;
+}
+
+size_t hc_scratch_bytes(hc_algo_t algo, int P, size_t count, hc_dtype_t dtype) {
+    if (!valid_algo(algo) || !valid_dtype(dtype) || P < 1 || P > kMaxRanks) return 0;
+    return (size_t)P * scratch_stride(count, dtype);
+}
+
+hc_status_t hc_schedule_stats(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_server,
+                              size_t count, hc_dtype_t dtype, size_t max_loop_bytes,
+                              hc_stats_t* stats, unsigned long long* bytes_sent) {
+    if (!valid_algo(algo) || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
+    if (P < 1 || P > kMaxRanks || count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
+    if (stats && stats->struct_size < sizeof(hc_stats_t)) return HC_ERR_INVALID_ARG;
+    int p_intra = algo == HC_ALGO_PIPELINE ? ranks_per_server : 1;
+    if (p_intra < 1 || P % p_intra) return HC_ERR_INVALID_ARG;
+    const int64_t n = (int64_t)count;
+    int spl = 0;
+    if (!schedule_traffic(algo, coll, P, p_intra, n, dtype, (int64_t)max_loop_bytes, &spl,
+                          bytes_sent))
+        return HC_ERR_INVALID_ARG;
+    if (!stats) return HC_OK;
+    Aliasing al;
+    for (int r = 0; r < P; r++) { al.orig_is_work[r] = true; al.final_is_work[r] = true; }
+    Plan plan;
+    if (!build_plan(algo, coll, P, p_intra, n, dtype, (int64_t)max_loop_bytes, al, &plan))
+        return HC_ERR_INVALID_ARG;
+    const int es = elem_bytes(dtype);
+    stats->steps_per_loop = spl;
+    stats->loops = plan.sl.loops;
+    stats->chunk = (size_t)plan.sl.chunk;
+    stats->tail = (size_t)plan.sl.tail;
+    stats->launches_step = (int)plan.launches.size();
+    stats->launches_fused = n > 0 ? 1 : 0;
+    unsigned long long sb = 0;
+    for (const PlanLaunch& L : plan.launches)
+        for (const DevItem& it : L.items)
+            for (int i = 0; i < it.seg_width * it.seg_reps; i++) {
+                int k = it.seg_first + (i / it.seg_width) * it.seg_stride + i % it.seg_width;
+                int64_t lo = std::min(plan.lay.seg_lo(k) + L.lo, plan.lay.seg_hi(k));
+                int64_t hi = std::min(plan.lay.seg_lo(k) + L.hi, plan.lay.seg_hi(k));
+                unsigned long long len = (unsigned long long)(hi - lo) * es;
+                sb += len * (unsigned long long)(it.in_cnt + (it.acc_rank >= 0) + it.out_cnt);
+            }
+    stats->step_bytes = sb;
+    const unsigned long long nb = (unsigned long long)n * es;
+    if (coll == HC_COLL_ALLREDUCE) stats->fused_bytes = 2ull * P * nb;
+    else if (coll == HC_COLL_REDUCE_SCATTER) stats->fused_bytes = (unsigned long long)(P + 1) * nb;
+    else stats->fused_bytes = (unsigned long long)(P + 1) * nb;
+    return HC_OK;
+}
+
+hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_server,
+                         size_t count, hc_dtype_t dtype, size_t max_loop_bytes, int in_place,
+                         hc_plan_record_t* records, size_t cap, size_t* n_out, int* launches) {
+    if (!valid_algo(algo) || !valid_coll(coll) || !valid_dtype(dtype) || !n_out)
+        return HC_ERR_INVALID_ARG;
+    if (P < 1 || P > kMaxRanks || count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
+    int p_intra = algo == HC_ALGO_PIPELINE ? ranks_per_server : 1;
+    if (p_intra < 1 || P % p_intra) return HC_ERR_INVALID_ARG;
+    Aliasing al;
+    for (int r = 0; r < P; r++) {
+        al.orig_is_work[r] = in_place != 0;
+        al.final_is_work[r] = in_place != 0;
+        if (coll == HC_COLL_ALLREDUCE) al.final_is_work[r] = true;
+        if (coll == HC_COLL_ALLGATHER) al.final_is_work[r] = true;
+    }
+    Plan plan;
+    if (!build_plan(algo, coll, P, p_intra, (int64_t)count, dtype, (int64_t)max_loop_bytes, al,
+                    &plan))
+        return HC_ERR_INVALID_ARG;
+    size_t m = 0;
+    for (size_t li = 0; li < plan.launches.size(); li++) {
+        const PlanLaunch& L = plan.launches[li];
+        for (const DevItem& it : L.items)
+            for (int i = 0; i < it.seg_width * it.seg_reps; i++) {
+                int k = it.seg_first + (i / it.seg_width) * it.seg_stride + i % it.seg_width;
+                if (records && m < cap) {
+                    hc_plan_record_t& R = records[m];
+                    std::memset(&R, 0, sizeof R);
+                    R.launch = (int32_t)li;
+                    R.seg = k;
+                    R.lo = std::min(plan.lay.seg_lo(k) + L.lo, plan.lay.seg_hi(k));
+                    R.hi = std::min(plan.lay.seg_lo(k) + L.hi, plan.lay.seg_hi(k));
+                    R.acc_rank = it.acc_rank;
+                    R.acc_loc = it.acc_loc;
+                    R.in_loc = it.in_loc;
+                    R.in_cnt = it.in_cnt;
+                    R.out_loc = it.out_loc;
+                    R.out_cnt = it.out_cnt;
+                    for (int j = 0; j < it.in_cnt; j++)
+                        R.in_ranks[j] = it.in_base + (it.in_rot + j) % it.in_mod;
+                    for (int j = 0; j < it.out_cnt; j++)
+                        R.out_ranks[j] = it.out_base + (it.out_rot + j) % it.out_mod;
+                }
+                m++;
+            }
+    }
+    *n_out = m;
+    if (launches) *launches = (int)plan.launches.size();
+    return HC_OK;
+}
+
+const char* hc_status_string(hc_status_t s) {
+    switch (s) {
+    case HC_OK: return "success";
+    case HC_ERR_INVALID_ARG: return "invalid argument";
+    case HC_ERR_UNSUPPORTED: return "unsupported combination";
+    case HC_ERR_ALIGN: return "device pointer not 16-byte aligned";
+    case HC_ERR_SCRATCH: return "step-mode scratch missing or too small";
+    case HC_ERR_CUDA: return "CUDA launch or query failed";
+    case HC_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+    }
+}
+
+int hc_version(void) { return HC_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,144 @@
+// hc_internal.h -- types shared by the host scheduler (hc_sched.cpp), the
+// C ABI (hc_api.cpp) and the kernels (hc_kernels.cu).  Not installed.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <vector>
+
+#include <cuda_runtime_api.h>
+
+#include "../../include/hc.h"
+
+namespace hc {
+
+constexpr int kMaxRanks = HC_MAX_RANKS;
+constexpr int kVecBytes = 16;  // one vector = 16 bytes = 4 x 32-bit or 8 x bf16
+
+// Buffer locations a step item can name, per rank.
+enum Loc : uint8_t {
+    LOC_ORIG = 0,   // the rank's input as handed in (send)
+    LOC_WORK = 1,   // working / output buffer (recv, or scratch for out-of-place RS)
+    LOC_FINAL = 2,  // ReduceScatter output segment (recv), global-indexed
+    LOC_COUNT = 3
+};
+
+inline int elem_bytes(hc_dtype_t dt) { return dt == HC_BFLOAT16 ? 2 : 4; }
+
+// ---------------------------------------------------------------------------
+// Segment layout: S segments of stride L (a multiple of 16 bytes); segment k
+// covers [min(kL, n), min((k+1)L, n)).
+// ---------------------------------------------------------------------------
+struct Layout {
+    int S = 0;
+    int64_t L = 0;
+    int64_t n = 0;
+    int A = 0;  // elements per 16-byte vector
+    int64_t seg_lo(int k) const { int64_t v = (int64_t)k * L; return v < n ? v : n; }
+    int64_t seg_hi(int k) const { int64_t v = (int64_t)(k + 1) * L; return v < n ? v : n; }
+};
+
+int num_segments(hc_algo_t algo, hc_coll_t coll, int P);
+Layout make_layout(hc_algo_t algo, hc_coll_t coll, int P, int64_t n, hc_dtype_t dt);
+
+struct Slicing {
+    int64_t chunk = 0;  // elements per segment per loop
+    int loops = 1;
+    int64_t tail = 0;
+};
+Slicing make_slicing(hc_algo_t algo, int P, int p_intra, const Layout& lay, hc_dtype_t dt,
+                     int64_t loop_bytes);
+
+// ---------------------------------------------------------------------------
+// Device step items.  An item computes, for every segment of its segment set
+// and every element j of the launch's slice of that segment,
+//     v = in[0][j] (+) in[1][j] (+) ... (+) in[cnt-1][j]      (left to right)
+//     if acc >= 0:  v = acc[j] (+) v                           (received on the left)
+//     out[o][j] = v  for every output o
+// A copy is an item with one input and no acc.  Rank sets are rotations:
+// member i of (base, rot, mod, cnt) is rank base + (rot + i) % mod.
+// Segment set: seg_first + (i / seg_width) * seg_stride + (i % seg_width),
+// i < seg_width * seg_reps.
+// ---------------------------------------------------------------------------
+struct DevItem {
+    int16_t out_base, out_rot, out_mod, out_cnt;
+    int16_t in_base, in_rot, in_mod, in_cnt;
+    int16_t acc_rank;  // -1 = none
+    uint8_t acc_loc, in_loc, out_loc, pad0;
+    int16_t seg_width, seg_reps;
+    int16_t pad1;
+    int32_t seg_first, seg_stride;
+    int32_t cta_begin;  // first CTA of this item in the launch grid
+};
+static_assert(sizeof(DevItem) == 40, "DevItem layout");
+
+// Kernel-parameter block of one step launch.  MAXI items at most.
+template <int MAXI>
+struct StepParams {
+    uintptr_t base[LOC_COUNT][kMaxRanks];  // element 0 of each rank's global-indexed view
+    int64_t L;        // segment stride (elements)
+    int64_t n;        // elements per rank vector
+    int64_t lo, hi;   // slice of every segment for this launch (relative to the segment start)
+    int64_t vecs;     // vectors per segment slice: ceil((hi - lo) / A)
+    int32_t nitems;
+    int32_t total_ctas;
+    DevItem items[MAXI];
+};
+
+// One launch of a step-mode plan: items + the slice they act on.
+struct PlanLaunch {
+    int64_t lo = 0, hi = 0;  // slice relative to segment start
+    std::vector<DevItem> items;
+    int step = 0, loop = 0;
+};
+
+struct Plan {
+    Layout lay;
+    Slicing sl;
+    int steps_per_loop = 0;
+    std::vector<PlanLaunch> launches;
+};
+
+// Which buffers alias, per rank (step-mode planning).
+struct Aliasing {
+    bool orig_is_work[kMaxRanks];   // in place: send and working buffer coincide
+    bool final_is_work[kMaxRanks];  // ReduceScatter in place: output segment is in the working buffer
+};
+
+// Build the step-mode plan (host only).  Returns false on bad arguments.
+bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n, hc_dtype_t dt,
+                int64_t loop_bytes, const Aliasing& alias, Plan* out);
+
+// Per-rank bytes sent over the whole schedule and steps per loop (host only).
+bool schedule_traffic(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n,
+                      hc_dtype_t dt, int64_t loop_bytes, int* steps_per_loop,
+                      unsigned long long* bytes_sent);
+
+// Assign CTAs to the items of a launch; returns the grid size.
+int assign_ctas(PlanLaunch& L, const Layout& lay, int threads, int max_ctas);
+
+// ---------------------------------------------------------------------------
+// Fused-mode launch description.
+// ---------------------------------------------------------------------------
+struct FusedArgs {
+    hc_algo_t algo;
+    hc_coll_t coll;
+    hc_dtype_t dtype;
+    hc_op_t op;
+    int P;
+    int p_intra;
+    int64_t n;
+    Layout lay;
+    const void* const* send;  // host array of P device pointers (may be null for in-place AG)
+    void* const* recv;
+    bool ag_in_place[kMaxRanks];
+    bool rs_in_place[kMaxRanks];
+};
+
+// Kernel launchers (hc_kernels.cu).
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count);
+cudaError_t launch_step(const Plan& plan, int P, hc_dtype_t dt, hc_op_t op,
+                        const uintptr_t (&base)[LOC_COUNT][kMaxRanks], cudaStream_t stream,
+                        int sm_count);
+
+}  // namespace hc

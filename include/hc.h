@@ -1,0 +1,246 @@
+/*
+ * hc.h -- C ABI of libhc: the data plane of HCCL-style AllReduce,
+ * ReduceScatter and AllGather schedules (Ring, Recursive Halving-Doubling,
+ * hierarchical Pipeline) for P virtual ranks whose buffers all live in the
+ * memory of one GPU (sm_103a).
+ *
+ * Sources (page title, section):
+ *  - "深入分析HCCL集合通信库中Ring AllReduce和Recursive Halving-Doubling…"
+ *    (mhpn.cn, Ring vs RHD on Ascend): "AllReduce的数学抽象与问题定义"
+ *    (definition Y[j] = sum_i X_i[j]), "Ring AllReduce带宽最优的环形流水线"
+ *    (RingAllReduce(self, ring[], send_buf, recv_buf, elem_count, dtype, op,
+ *    comm) and its reduce_op loop), "Recursive Halving-Doubling短消息场景的
+ *    延迟优势", and "Ascend950的AIV/AICPU通信引擎与图模式" (HcclResult status
+ *    convention of HcclGraphAddAllReduce).
+ *  - HCCL topology / AllReduce / fault-recovery article (hwcomputing.csdn.net),
+ *    "AllReduce算法实现" (Scatter-Reduce + AllGather, 128-byte chunking) and
+ *    "梯度同步与计算重叠" (stream-ordered asynchronous collectives).
+ *  - "HCCL RHD（Recursive Halving-Doubling）算法深度解析", "算法描述" and
+ *    Table 1 (non-power-of-two fold, ReduceScatter keeping scatter order).
+ *  - "HCCL Pipeline分级流水算法深度解析", "AllGather 算子的 Pipeline 时序编排",
+ *    "Rank0 视角的传输任务编排" (LocalCopy only when input and output
+ *    differ), "源码中的流水执行印证" (loops sized by a scratch limit, tail
+ *    slice) and Table 1.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - P virtual ranks, 1 <= P <= HC_MAX_RANKS.  `send` and `recv` are host
+ *    arrays of P device pointers (read during the call only; the library keeps
+ *    no reference to them).  The caller owns every buffer and the scratch;
+ *    the library allocates no device memory.
+ *  - `count` is n, the number of elements of one rank's full vector, for all
+ *    three collectives.  Segment k of a vector is [off_k, off_k + len_k) as
+ *    returned by hc_segment_range(): L = ceil(n / S) rounded up to a multiple
+ *    of 16 bytes, off_k = min(k L, n), len_k = min((k+1) L, n) - off_k, with
+ *    S = P segments (S = 2^floor(log2 P) for the RHD AllReduce).  Trailing
+ *    segments may be short or empty.
+ *  - Every device pointer must be 16-byte aligned (HC_ERR_ALIGN otherwise).
+ *    Buffers of different ranks must not overlap; a rank's send and recv are
+ *    either disjoint or exactly "in place" as defined per collective.
+ *  - Every call is asynchronous on `stream` (NULL = legacy default stream)
+ *    and may be captured into a CUDA graph.  All validation happens before
+ *    any launch: a non-HC_OK status means nothing was launched.  Faults of
+ *    the kernels themselves surface at the next synchronisation.
+ *  - count == 0 returns HC_OK and launches nothing.
+ *  - Reduction semantics per element and per schedule step, acc (+) x:
+ *      int32  sum/prod wrap modulo 2^32, max/min by signed compare;
+ *      fp32   IEEE binary32 round-to-nearest-even, no FMA, no flush to zero;
+ *      bf16   both operands widened to binary32, op applied, result rounded
+ *             to bf16 (nearest even) after every step;
+ *      max/min of fp32/bf16 follow IEEE 754 totalOrder (-0 < +0), so they are
+ *             exact and independent of the schedule.
+ *    Sum/prod of fp32/bf16 depend on association order; each (algo, mode)
+ *    reproduces exactly the order its schedule implies:
+ *      Ring      segment k: ((X_{k+1} (+) X_{k+2}) (+) ...) (+) X_k;
+ *      RHD       folded pairs u_i = X_{2i} (+) X_{2i+1} (i < P - 2^floor(log2 P)),
+ *                then a balanced pairwise tree over the 2^floor(log2 P)
+ *                leaves in rank order (partner bit 0 first);
+ *      Pipeline  segment (s,l): intra-server partials
+ *                I_t = X_(t,l) (+) X_(t,l+1) (+) ... (rotated from l),
+ *                then I_{s+1} (+) I_{s+2} (+) ... (+) I_s around the
+ *                inter-server ring (rank = server * ranks_per_server + local).
+ *  - Not thread-safe: calls from several host threads must be serialised by
+ *    the caller (the library keeps a small host-side cache).
+ */
+#ifndef HC_H
+#define HC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define HC_MAX_RANKS 64
+#define HC_VERSION 1
+
+/* Same object as cudaStream_t / CUstream. */
+typedef struct CUstream_st* hc_stream_t;
+
+/* Status codes, after HcclResult / HCCL_SUCCESS. */
+typedef enum {
+    HC_OK = 0,
+    HC_ERR_INVALID_ARG = 1,   /* null pointer, P out of range, overlap, bad enum value */
+    HC_ERR_UNSUPPORTED = 2,   /* dtype x op or algo x option combination not provided */
+    HC_ERR_ALIGN = 3,         /* a device pointer is not 16-byte aligned */
+    HC_ERR_SCRATCH = 4,       /* step-mode scratch missing or too small */
+    HC_ERR_CUDA = 5,          /* a CUDA launch or query failed */
+    HC_ERR_TIMEOUT = 6        /* reserved: a bounded device-side wait gave up */
+} hc_status_t;
+
+typedef enum { HC_INT32 = 0, HC_FLOAT32 = 1, HC_BFLOAT16 = 2 } hc_dtype_t;
+typedef enum { HC_SUM = 0, HC_PROD = 1, HC_MAX = 2, HC_MIN = 3 } hc_op_t;
+typedef enum { HC_ALGO_RING = 0, HC_ALGO_RHD = 1, HC_ALGO_PIPELINE = 2 } hc_algo_t;
+typedef enum { HC_COLL_ALLREDUCE = 0, HC_COLL_REDUCE_SCATTER = 1, HC_COLL_ALLGATHER = 2 } hc_coll_t;
+
+/*
+ * HC_MODE_FUSED: one kernel reads every rank's element once, reduces it in
+ *   registers in the schedule's association order and writes every output
+ *   (minimum traffic: AllReduce reads P n b and writes P n b bytes).
+ * HC_MODE_STEP: one kernel launch per schedule step (and per loop), each a
+ *   16-byte vectorised segment reduce / copy over all ranks, i.e. the steps
+ *   run as the pages describe them, with the peers' buffers read directly.
+ * Both modes give bit-identical results.
+ */
+typedef enum { HC_MODE_FUSED = 0, HC_MODE_STEP = 1 } hc_mode_t;
+
+/*
+ * Options; pass NULL for the defaults (fused, ranks_per_server 1, one loop,
+ * no scratch).  struct_size must be sizeof(hc_opts_t).
+ *  ranks_per_server : Pipeline only: ranks per server (p_intra); P must be a
+ *                     multiple of it; rank = server * p_intra + local.
+ *  max_loop_bytes   : step mode: byte limit per loop (the pages' scratch
+ *                     limit maxTmpMemSize_); each segment is cut into slices
+ *                     of c = align_down(max_loop_bytes / (P * slots * b),
+ *                     128 / b) elements (slots = 1 Ring, ceil(P/2) RHD,
+ *                     max(1, p_intra - 1) Pipeline) and the schedule runs once
+ *                     per slice; 0 = one loop.  Results do not depend on it.
+ *  scratch          : step mode, out-of-place ReduceScatter only: device
+ *                     memory of at least hc_scratch_bytes() bytes, 16-byte
+ *                     aligned, holding the ranks' intermediate partial sums.
+ *                     Its contents on entry are ignored and on exit undefined.
+ */
+typedef struct {
+    size_t struct_size;
+    hc_mode_t mode;
+    int ranks_per_server;
+    size_t max_loop_bytes;
+    void* scratch;
+    size_t scratch_bytes;
+} hc_opts_t;
+
+/*
+ * AllReduce: recv[r][j] = (+)_i send[i][j] for every rank r and j < count.
+ * ("AllReduce的数学抽象与问题定义"; Ring: "Ring AllReduce带宽最优的环形流水线";
+ * RHD: RHD article "算法描述" / Table 1 Allreduce row; Pipeline: Pipeline
+ * article Table 1 AllReduce row.)
+ *  send[r] : device pointer, count elements of rank r's input.
+ *  recv[r] : device pointer, count elements of rank r's output;
+ *            recv[r] == send[r] means in place (send[r] is overwritten).
+ */
+hc_status_t hc_allreduce(const void* const* send, void* const* recv, int P, size_t count,
+                         hc_dtype_t dtype, hc_op_t op, hc_algo_t algo,
+                         const hc_opts_t* opts, hc_stream_t stream);
+
+/*
+ * ReduceScatter: recv[r][0 .. len_r) = segment r of (+)_i send[i], where
+ * (off_r, len_r) = hc_segment_range(algo, HC_COLL_REDUCE_SCATTER, ...).
+ * (Ring: reduce-scatter phase of "Ring AllReduce带宽最优的环形流水线"; RHD:
+ * Table 1 ReduceScatter row, scatter order kept; Pipeline: Table 1
+ * ReduceScatter row.)
+ *  send[r] : count elements of rank r's input.
+ *  recv[r] : len_r elements; recv[r] == send[r] + off_r means in place (then
+ *            all of send[r] is used as working memory and overwritten).
+ *  Step mode with any out-of-place rank needs opts->scratch.
+ */
+hc_status_t hc_reduce_scatter(const void* const* send, void* const* recv, int P, size_t count,
+                              hc_dtype_t dtype, hc_op_t op, hc_algo_t algo,
+                              const hc_opts_t* opts, hc_stream_t stream);
+
+/*
+ * AllGather: recv[r][off_k .. off_k + len_k) = send[k][0 .. len_k) for every
+ * rank r and segment k.  (Ring: all-gather phase; RHD: Table 1 AllGather row;
+ * Pipeline: "AllGather 算子的 Pipeline 时序编排", LocalCopy of "Rank0 视角".)
+ *  send    : NULL, or P pointers; send[k] holds len_k elements of segment k;
+ *            send == NULL or send[k] == recv[k] + off_k means in place (the
+ *            segment is already at its place in recv[k]).
+ *  recv[r] : count elements.
+ */
+hc_status_t hc_allgather(const void* const* send, void* const* recv, int P, size_t count,
+                         hc_dtype_t dtype, hc_algo_t algo,
+                         const hc_opts_t* opts, hc_stream_t stream);
+
+/* Segment k's element range (see the layout rule above).  k < S, where
+ * S = hc_num_segments(algo, coll, P). */
+hc_status_t hc_segment_range(hc_algo_t algo, hc_coll_t coll, int P, size_t count,
+                             hc_dtype_t dtype, int k, size_t* off, size_t* len);
+int hc_num_segments(hc_algo_t algo, hc_coll_t coll, int P);
+
+/* Scratch bytes a step-mode, out-of-place ReduceScatter needs. */
+size_t hc_scratch_bytes(hc_algo_t algo, int P, size_t count, hc_dtype_t dtype);
+
+/*
+ * Schedule statistics (host only, no GPU needed).
+ *  steps_per_loop : communication steps of one loop (Ring AllReduce 2(P-1),
+ *                   RHD 2 ceil(log2 P), Pipeline 2 p_inter, ...)
+ *  loops, chunk, tail : the loop slicer's result (elements per segment)
+ *  launches_step  : kernels one step-mode call launches (in place)
+ *  launches_fused : kernels one fused-mode call launches
+ *  step_bytes     : bytes the step-mode kernels read + write (in place)
+ *  fused_bytes    : bytes the fused kernel reads + writes (out of place)
+ *  bytes_sent     : optional array of P: bytes each rank sends to other ranks
+ *                   over the whole schedule (the pages' per-rank traffic)
+ */
+typedef struct {
+    size_t struct_size;
+    int steps_per_loop;
+    int loops;
+    size_t chunk;
+    size_t tail;
+    int launches_step;
+    int launches_fused;
+    unsigned long long step_bytes;
+    unsigned long long fused_bytes;
+} hc_stats_t;
+
+hc_status_t hc_schedule_stats(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_server,
+                              size_t count, hc_dtype_t dtype, size_t max_loop_bytes,
+                              hc_stats_t* stats, unsigned long long* bytes_sent);
+
+/*
+ * Step-plan export for host-side checking (no GPU needed): the work each
+ * step-mode launch performs, one record per (launch, item, segment).  With
+ * cap == 0 or records == NULL only the number of records is returned in *n.
+ * Locations: 0 = the rank's input (send), 1 = its working/output buffer
+ * (recv, or the scratch for an out-of-place ReduceScatter), 2 = its
+ * ReduceScatter output (recv).  Every record computes, for lo <= j < hi,
+ *   out[o][j] = (acc (+)) in[0][j] (+) in[1][j] (+) ... for each o in outs.
+ * `in_place` says which buffers alias (nonzero: every rank in place).
+ */
+typedef struct {
+    int32_t launch;
+    int32_t seg;
+    int64_t lo, hi;
+    int32_t acc_rank;   /* -1: no left operand */
+    int32_t acc_loc;
+    int32_t in_loc;
+    int32_t in_cnt;
+    int32_t out_loc;
+    int32_t out_cnt;
+    int32_t in_ranks[HC_MAX_RANKS];
+    int32_t out_ranks[HC_MAX_RANKS];
+} hc_plan_record_t;
+
+hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_server,
+                         size_t count, hc_dtype_t dtype, size_t max_loop_bytes, int in_place,
+                         hc_plan_record_t* records, size_t cap, size_t* n, int* launches);
+
+const char* hc_status_string(hc_status_t status);
+int hc_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HC_H */

@@ -1,0 +1,171 @@
+"""GPU parity: every algorithm x collective x dtype x op x mode, in place and
+out of place, compared with the oracle's step-by-step replay element by
+element, bit for bit, at sizes that span several tiles and a ragged tail;
+plus the edge cases (empty input, P = 1, the maximum P = 64, one element).
+All calls go through the C ABI (libhc.so)."""
+import numpy as np
+import pytest
+
+import hc_inputs
+import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from collective_communication_algorithms_gb300 import build
+    build.build()
+    from collective_communication_algorithms_gb300 import _binding as B
+    return B.lib()
+
+
+from gpu_util import expected, run_collective, same_bits, segments  # noqa: E402
+
+ALGOS = ("ring", "rhd", "pipeline")
+COLLS = ("allreduce", "reducescatter", "allgather")
+DTYPES = ("int32", "float32", "bfloat16")
+
+
+def intra_for(algo, P):
+    if algo != "pipeline":
+        return 1
+    for d in (8, 4, 3, 2):
+        if P % d == 0 and P // d >= 2:
+            return d
+    return 1
+
+
+def inputs(dtype, P, n, seed, op):
+    if dtype == "int32":
+        X = hc_inputs.uniform_int32(P, n, seed=seed)
+        return (X % 5 + 1).astype(np.int32) if op == "prod" else X
+    scale = 1.0
+    X = hc_inputs.rank_buffers(dtype, P, n, seed=seed, scale=scale)
+    if op == "prod" and dtype == "float32":
+        X = (np.float32(1) + X * np.float32(0.01)).astype(np.float32)
+    if op == "prod" and dtype == "bfloat16":
+        X = hc_inputs.gradients_bf16(P, n, seed=seed, scale=0.01)
+        X = (X.astype(np.uint32) | 0).astype(np.uint16)  # values near 0: product underflows gracefully
+    return X
+
+
+def check(coll, algo, X, dtype, op, mode, in_place, p_intra=1, loop_bytes=0):
+    P, n = X.shape
+    res, guards = run_collective(coll, algo, X, dtype, op, mode, in_place, p_intra, loop_bytes)
+    assert guards, "a write landed outside its buffer"
+    Y = O.replay(algo, coll, X, op, dtype, p_intra=p_intra, loop_bytes=loop_bytes)
+    want = expected(coll, Y, segments(algo, coll, P, n, dtype))
+    for r in range(P):
+        if not same_bits(res[r], want[r], dtype):
+            a = res[r].view(np.int32 if dtype != "bfloat16" else np.int16)
+            b = np.ascontiguousarray(want[r]).view(a.dtype)
+            bad = np.nonzero(a != b)[0]
+            raise AssertionError("%s %s %s %s %s P=%d n=%d rank %d: %d mismatches, first at %d"
+                                 % (algo, coll, dtype, op, mode, P, n, r, bad.size, bad[0]))
+
+
+SIZES = (1, 37, 4099, 65536 + 12)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("mode", ["fused", "step"])
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("op", ["sum", "prod", "max", "min"])
+def test_allreduce(algo, mode, dtype, op):
+    for P in (2, 3, 5, 8, 12):
+        pin = intra_for(algo, P)
+        for n in SIZES:
+            X = inputs(dtype, P, n, seed=P * 7 + n, op=op)
+            for in_place in (False, True):
+                check("allreduce", algo, X, dtype, op, mode, in_place, pin)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("mode", ["fused", "step"])
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("coll", ["reducescatter", "allgather"])
+def test_reducescatter_allgather(algo, mode, dtype, coll):
+    for P in (2, 3, 5, 8, 12, 16):
+        pin = intra_for(algo, P)
+        for n in SIZES:
+            X = inputs(dtype, P, n, seed=P * 11 + n, op="sum")
+            for in_place in (False, True):
+                check(coll, algo, X, dtype, "sum", mode, in_place, pin)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("coll", COLLS)
+def test_step_mode_loops(algo, coll):
+    """Several loops with a tail slice; results equal the oracle's (which does
+    not depend on the loops either)."""
+    P = 8 if algo != "pipeline" else 8
+    pin = intra_for(algo, P)
+    n = 200003
+    X = hc_inputs.gradients_f32(P, n, seed=3)
+    for lb in (65536, 1 << 20):
+        for in_place in (False, True):
+            check(coll, algo, X, "float32", "sum", "step", in_place, pin, loop_bytes=lb)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("mode", ["fused", "step"])
+def test_single_rank_and_max_ranks(algo, mode):
+    for P in (1, 64):
+        pin = intra_for(algo, P)
+        for coll in COLLS:
+            X = hc_inputs.gradients_f32(P, 3000, seed=P)
+            for in_place in (False, True):
+                check(coll, algo, X, "float32", "sum", mode, in_place, pin)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_contribution_counting_int32(algo):
+    """X_i = 2^i: every output is 2^P - 1 iff every rank contributed once."""
+    for P in (2, 5, 8, 12, 16, 24, 30):
+        pin = intra_for(algo, P)
+        n = 4096 + 4
+        X = np.tile((1 << np.arange(P, dtype=np.int64)).astype(np.int32)[:, None], (1, n))
+        for mode in ("fused", "step"):
+            res, ok = run_collective("allreduce", algo, X, "int32", "sum", mode, False, pin)
+            assert ok
+            for r in range(P):
+                assert np.all(res[r].view(np.int32) == (1 << P) - 1), (algo, mode, P, r)
+
+
+def test_empty_input_is_noop():
+    from collective_communication_algorithms_gb300 import _binding as B
+    B.hc_allreduce(None, None, 4, 0, "float32", "sum", "ring")
+    B.hc_reduce_scatter(None, None, 4, 0, "float32", "sum", "rhd")
+    B.hc_allgather(None, None, 4, 0, "float32", "pipeline")
+
+
+def test_fused_and_step_agree_bitwise_tree_discriminating():
+    """fp32 inputs mixing 2^24-scale values and small ones: any change of the
+    association order shows up in low bits."""
+    P, n = 12, 8192
+    rng = np.random.default_rng(5)
+    X = (rng.standard_normal((P, n)) * np.exp2(rng.integers(-20, 24, (P, n)))).astype(np.float32)
+    for algo in ALGOS:
+        pin = intra_for(algo, P)
+        a, _ = run_collective("allreduce", algo, X, "float32", "sum", "fused", False, pin)
+        b, _ = run_collective("allreduce", algo, X, "float32", "sum", "step", False, pin)
+        for r in range(P):
+            assert same_bits(a[r], b[r], "float32")
+        check("allreduce", algo, X, "float32", "sum", "fused", False, pin)
+
+
+def test_uses_the_given_stream():
+    P, n = 4, 100000
+    X = hc_inputs.gradients_f32(P, n, seed=1)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        res, ok = run_collective("allreduce", "ring", X, "float32", "sum", "fused", False, 1,
+                                 0, stream=s.cuda_stream)
+    assert ok
+    Y = O.replay("ring", "allreduce", X, "sum", "float32")
+    assert same_bits(res[0], Y[0], "float32")

@@ -1,0 +1,399 @@
+"""Host-side checks of libhc (no GPU needed): the C ABI loads and exports every
+symbol include/hc.h declares; its segment layout, loop slicer, step counts
+and per-rank traffic equal the oracle's (independent implementations of the
+same reading); its step plans are free of intra-launch races and, executed on
+the CPU record by record, give the oracle's results and association trees;
+invalid arguments are rejected before any launch.
+"""
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import hc_inputs
+import oracle as O
+from collective_communication_algorithms_gb300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+ALGOS = ("ring", "rhd", "pipeline")
+COLLS = ("allreduce", "reducescatter", "allgather")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from collective_communication_algorithms_gb300 import build
+    build.build()
+    return B.lib()
+
+
+def intra_for(algo, P):
+    if algo != "pipeline":
+        return 1
+    for d in (8, 4, 3, 2):
+        if P % d == 0 and P // d >= 2:
+            return d
+    return 1
+
+
+def test_exports_every_declared_symbol():
+    header = open(os.path.join(ROOT, "include", "hc.h")).read()
+    declared = set(re.findall(r"^\s*(?:[a-z_ ]+\*?\s+)?\**\s*(hc_[a-z_]+)\s*\(", header, re.M))
+    declared |= set(re.findall(r"\b(hc_[a-z_]+)\s*\(", header))
+    declared = {d for d in declared if not d.endswith("_t")}
+    assert declared == set(B.EXPORTS), declared ^ set(B.EXPORTS)
+    for name in declared:
+        assert hasattr(B.lib(), name), name
+    assert B.hc_version() == 1
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("coll", COLLS)
+@pytest.mark.parametrize("dtype", ["int32", "float32", "bfloat16"])
+def test_layout_equals_oracle(algo, coll, dtype):
+    for P in (1, 2, 3, 5, 8, 12, 16, 32, 64):
+        assert B.hc_num_segments(algo, coll, P) == O.num_segments(algo, coll, P)
+        for n in (0, 1, 5, 100, 4097, 1 << 20):
+            S = O.num_segments(algo, coll, P)
+            for k in range(S):
+                assert B.hc_segment_range(algo, coll, P, n, dtype, k) == O.segment(algo, coll, P, n, dtype, k)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+def test_slicer_equals_oracle(algo):
+    for P in (2, 5, 8, 12, 32):
+        pin = intra_for(algo, P)
+        for n in (1000, 77777, 8388608):
+            for lb in (0, 4096, 1 << 16, 1 << 20, 64 << 20):
+                st, _ = B.hc_schedule_stats(algo, "allreduce", P, n, "float32", pin, lb)
+                c, loops, tail = O.slicer(algo, "allreduce", P, n, "float32", lb, p_intra=pin)
+                assert (st["chunk"], st["loops"], st["tail"]) == (c, loops, tail)
+
+
+def test_slicer_pipeline_4x8_64MiB():
+    st, _ = B.hc_schedule_stats("pipeline", "allreduce", 32, 8388608, "float32", 8, 64 << 20)
+    assert (st["chunk"], st["loops"], st["tail"]) == (74880, 4, 37504)
+    assert st["steps_per_loop"] == 8
+    assert st["launches_step"] == 4 * 8
+    assert st["fused_bytes"] == 2 * 32 * 8388608 * 4
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("coll", COLLS)
+def test_steps_and_traffic_equal_oracle(algo, coll):
+    for P in (1, 2, 3, 4, 5, 6, 8, 12, 16, 24, 32, 64):
+        pin = intra_for(algo, P)
+        n = 16 * P + 3
+        st, sent = B.hc_schedule_stats(algo, coll, P, n, "float32", pin, 0)
+        msgs, spl, _ = O.schedule(algo, coll, P, n, "float32", p_intra=pin)
+        assert st["steps_per_loop"] == spl, (algo, coll, P)
+        want = np.zeros(P, dtype=np.int64)
+        np.add.at(want, msgs["src"], (msgs["hi"] - msgs["lo"]) * 4)
+        assert list(want) == sent, (algo, coll, P)
+
+
+def test_ring_traffic_and_step_bytes_closed_forms():
+    P, n = 8, 16777216
+    st, sent = B.hc_schedule_stats("ring", "allreduce", P, n, "float32")
+    assert st["steps_per_loop"] == 14
+    assert all(s == 2 * (P - 1) * n // P * 4 for s in sent)
+    # step mode moves 5 (P-1) n b bytes: RS steps read 2 / write 1, AG steps read 1 / write 1
+    assert st["step_bytes"] == 5 * (P - 1) * n * 4
+    st, _ = B.hc_schedule_stats("rhd", "allreduce", 8, n, "float32")
+    assert st["steps_per_loop"] == 6 and st["step_bytes"] == 5 * 7 * n * 4
+
+
+# ---------------------------------------------------------------------------
+# step plans: race freedom and CPU execution
+# ---------------------------------------------------------------------------
+def records_by_launch(recs):
+    out = {}
+    for r in recs:
+        out.setdefault(r["launch"], []).append(r)
+    return [out[k] for k in sorted(out)]
+
+
+def physical(loc, rank, coll, in_place):
+    """Memory identity of a (location, rank) pair: locations that alias in
+    place map to the same buffer."""
+    if in_place:
+        return ("rank", rank)
+    if coll == "allreduce" or coll == "allgather":
+        return ("orig" if loc == 0 else "work", rank)
+    return ({0: "orig", 1: "work", 2: "final"}[loc], rank)
+
+
+def check_races(recs, coll, in_place):
+    for L in records_by_launch(recs):
+        writes = []
+        for i, r in enumerate(L):
+            for o in r["out_ranks"]:
+                writes.append((physical(r["out_loc"], o, coll, in_place), r["lo"], r["hi"], i))
+        for i, r in enumerate(L):
+            reads = [(physical(r["in_loc"], x, coll, in_place), r["lo"], r["hi"]) for x in r["in_ranks"]]
+            if r["acc_rank"] >= 0:
+                reads.append((physical(r["acc_loc"], r["acc_rank"], coll, in_place), r["lo"], r["hi"]))
+            for buf, lo, hi in reads:
+                for wb, wlo, whi, wi in writes:
+                    if wi != i and wb == buf and lo < whi and wlo < hi:
+                        raise AssertionError("read/write race in launch %d" % r["launch"])
+        ws = sorted(writes, key=lambda w: (w[0], w[1]))
+        for a, b in zip(ws, ws[1:]):
+            if a[0] == b[0] and b[1] < a[2] and a[3] != b[3]:
+                raise AssertionError("write/write race")
+
+
+def check_bounds(recs, algo, coll, P, n, dtype):
+    """Every record stays inside its segment (hence inside the rank vector),
+    names valid ranks, and reads a rank's input (location 0) of an
+    AllGather only inside that rank's own segment."""
+    segs = O.segments(algo, coll, P, n, dtype)
+    for r in recs:
+        off, ln = segs[r["seg"]]
+        assert off <= r["lo"] <= r["hi"] <= off + ln <= n
+        ranks = r["in_ranks"] + r["out_ranks"] + ([r["acc_rank"]] if r["acc_rank"] >= 0 else [])
+        assert all(0 <= x < P for x in ranks)
+        assert 1 <= len(r["in_ranks"]) and 1 <= len(r["out_ranks"])
+        if coll == "allgather" and r["in_loc"] == 0:
+            assert r["in_ranks"] == [r["seg"]]
+        if coll == "reducescatter" and r["out_loc"] == 2:
+            assert r["out_ranks"] == [r["seg"]]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("coll", COLLS)
+@pytest.mark.parametrize("in_place", [True, False])
+def test_step_plans_have_no_intra_launch_races(algo, coll, in_place):
+    for P in (1, 2, 3, 4, 5, 6, 8, 9, 12, 16, 64):
+        pin = intra_for(algo, P)
+        for n in (1, 37, 1000 * P + 7):
+            for lb in (0, 4096):
+                recs, _ = B.hc_step_plan(algo, coll, P, n, "float32", pin, lb, in_place)
+                check_races(recs, coll, in_place)
+                check_bounds(recs, algo, coll, P, n, "float32")
+
+
+class Buffers:
+    """CPU stand-in for the rank buffers a step plan addresses, with the
+    aliasing of an in-place or out-of-place call."""
+
+    def __init__(self, coll, X, in_place, segs, fill):
+        P, n = X.shape
+        self.orig = [X[r].copy() for r in range(P)]
+        if in_place:
+            self.work = self.orig
+            self.final = self.orig
+        else:
+            self.work = [np.full(n, fill, dtype=X.dtype) if X.dtype != object else
+                         np.array([None] * n, dtype=object) for _ in range(P)]
+            self.final = self.work if coll != "reducescatter" else [
+                np.full(n, fill, dtype=X.dtype) if X.dtype != object else
+                np.array([None] * n, dtype=object) for _ in range(P)]
+        if coll == "allgather" and not in_place:
+            # the input holds only the own segment
+            for r in range(P):
+                off, ln = segs[r]
+                keep = self.orig[r][off:off + ln].copy()
+                self.orig[r][:] = fill if X.dtype != object else None
+                self.orig[r][off:off + ln] = keep
+
+    def at(self, loc, rank):
+        return (self.orig, self.work, self.final)[loc][rank]
+
+
+def execute(recs, bufs, combine, shuffle_seed=0):
+    rnd = random.Random(shuffle_seed)
+    for L in records_by_launch(recs):
+        L = list(L)
+        rnd.shuffle(L)  # items of a launch run in no particular order
+        for r in L:
+            lo, hi = r["lo"], r["hi"]
+            if hi <= lo:
+                continue
+            v = bufs.at(r["in_loc"], r["in_ranks"][0])[lo:hi].copy()
+            for x in r["in_ranks"][1:]:
+                v = combine(v, bufs.at(r["in_loc"], x)[lo:hi])
+            if r["acc_rank"] >= 0:
+                v = combine(bufs.at(r["acc_loc"], r["acc_rank"])[lo:hi], v)
+            for o in r["out_ranks"]:
+                bufs.at(r["out_loc"], o)[lo:hi] = v
+
+
+def results(bufs, coll, P, segs):
+    if coll == "reducescatter":
+        return [bufs.final[r][segs[r][0]:segs[r][0] + segs[r][1]] for r in range(P)]
+    return [bufs.work[r] for r in range(P)]
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("coll", COLLS)
+@pytest.mark.parametrize("in_place", [True, False])
+def test_step_plan_executes_to_oracle_int32(algo, coll, in_place):
+    for P in (1, 2, 3, 5, 8, 12):
+        pin = intra_for(algo, P)
+        for n, lb in ((37, 0), (1000, 0), (4099, 512)):
+            X = hc_inputs.uniform_int32(P, n, seed=P + n)
+            segs = O.segments(algo, coll, P, n, "int32")
+            recs, _ = B.hc_step_plan(algo, coll, P, n, "int32", pin, lb, in_place)
+            bufs = Buffers(coll, X, in_place, segs, fill=-7)
+            execute(recs, bufs, lambda a, b: (a + b).astype(np.int32), shuffle_seed=P)
+            Y = O.replay(algo, coll, X, "sum", "int32", p_intra=pin, loop_bytes=lb)
+            got = results(bufs, coll, P, segs)
+            for r in range(P):
+                want = Y[r] if coll != "reducescatter" else Y[r, segs[r][0]:segs[r][0] + segs[r][1]]
+                np.testing.assert_array_equal(got[r], want, err_msg=str((algo, coll, P, n, r)))
+
+
+def canon(t):
+    if isinstance(t, tuple):
+        a, b = canon(t[0]), canon(t[1])
+        return (a, b) if repr(a) <= repr(b) else (b, a)
+    return t
+
+
+def parse(s):
+    """Oracle expression string -> nested tuples."""
+    s = s.replace("X", "")
+    tok = re.findall(r"\(|\)|\+|\d+|\?", s)
+    pos = 0
+
+    def rec():
+        nonlocal pos
+        t = tok[pos]
+        pos += 1
+        if t == "(":
+            a = rec()
+            pos += 1  # '+'
+            b = rec()
+            pos += 1  # ')'
+            return (a, b)
+        return int(t)
+    return rec()
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("coll", ["allreduce", "reducescatter"])
+def test_step_plan_trees_equal_oracle(algo, coll):
+    """Symbolic execution of the product's step plan gives the same
+    association tree, element by element, as the oracle's replay."""
+    for P in (2, 3, 4, 5, 6, 7, 8, 12, 16):
+        pin = intra_for(algo, P)
+        S = O.num_segments(algo, coll, P)
+        n = 4 * S
+        X = np.empty((P, n), dtype=object)
+        for r in range(P):
+            for j in range(n):
+                X[r, j] = r
+        segs = O.segments(algo, coll, P, n, "float32")
+        recs, _ = B.hc_step_plan(algo, coll, P, n, "float32", pin, 0, True)
+        bufs = Buffers(coll, X, True, segs, fill=None)
+
+        def combine(a, b):
+            out = np.empty(len(a), dtype=object)
+            for i in range(len(a)):
+                out[i] = (a[i], b[i])
+            return out
+        execute(recs, bufs, combine)
+        O.sym_reset()
+        Y = O.replay_sym(algo, coll, P, n, p_intra=pin)
+        rows = [(r, r) for r in range(P)] if coll == "reducescatter" else \
+            [(r, k) for r in range(P) for k in range(S)]
+        for r, k in rows:
+            off, ln = segs[k]
+            if ln == 0:
+                continue
+            got = canon(bufs.work[r][off])
+            want = canon(parse(O.sym_string(Y[r, off])))
+            assert got == want, (algo, coll, P, r, k)
+
+
+# ---------------------------------------------------------------------------
+# argument validation (fake, never-dereferenced pointers; host only)
+# ---------------------------------------------------------------------------
+def _no_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except Exception:
+        return True
+
+
+host_only = pytest.mark.skipif(not _no_gpu(), reason="uses fake device pointers")
+BASE = 1 << 40
+MB = 1 << 20
+
+
+def fake(P, stride=MB, base=BASE):
+    return [base + r * stride for r in range(P)]
+
+
+def status_of(fn, *args, **kw):
+    try:
+        fn(*args, **kw)
+        return 0
+    except B.HcError as e:
+        return e.status
+
+
+@host_only
+def test_rejects_bad_arguments_before_launch():
+    P, n = 4, 1024
+    s, d = fake(P), fake(P, base=BASE + 64 * MB)
+    INV, ALN, SCR = 1, 3, 4
+    assert status_of(B.hc_allreduce, s, d, 0, n, "float32", "sum", "ring") == INV
+    assert status_of(B.hc_allreduce, s, d, 65, n, "float32", "sum", "ring") == INV
+    assert status_of(B.hc_allreduce, s, d, P, n, 7, "sum", "ring") == INV
+    assert status_of(B.hc_allreduce, s, d, P, n, "float32", 9, "ring") == INV
+    assert status_of(B.hc_allreduce, s, d, P, n, "float32", "sum", 5) == INV
+    assert status_of(B.hc_allreduce, None, d, P, n, "float32", "sum", "ring") == INV
+    assert status_of(B.hc_allreduce, s, s[:2] + [0, s[3]], P, n, "float32", "sum", "ring") == INV
+    bad = list(d)
+    bad[2] += 4
+    assert status_of(B.hc_allreduce, s, bad, P, n, "float32", "sum", "ring") == ALN
+    # overlapping ranks: rank 1's output overlaps rank 0's
+    ov = list(d)
+    ov[1] = d[0] + 1024
+    assert status_of(B.hc_allreduce, s, ov, P, n, "float32", "sum", "ring") == INV
+    # send and recv of a rank partly overlap (neither disjoint nor in place)
+    part = list(d)
+    part[0] = s[0] + 512
+    assert status_of(B.hc_allreduce, s, part, P, n, "float32", "sum", "ring") == INV
+    # Pipeline: P must be a multiple of ranks_per_server
+    o = B.make_opts("fused", ranks_per_server=3)
+    assert status_of(B.hc_allreduce, s, d, P, n, "float32", "sum", "pipeline", o) == INV
+    o = B.make_opts(5)
+    assert status_of(B.hc_allreduce, s, d, P, n, "float32", "sum", "ring", o) == INV
+    # step-mode out-of-place ReduceScatter needs scratch of P * roundup(n b, 256)
+    need = B.hc_scratch_bytes("ring", P, n, "float32")
+    assert need == P * n * 4
+    rs_out = fake(P, base=BASE + 128 * MB)
+    o = B.make_opts("step")
+    assert status_of(B.hc_reduce_scatter, s, rs_out, P, n, "float32", "sum", "ring", o) == SCR
+    o = B.make_opts("step", scratch=BASE + 256 * MB, scratch_bytes=need - 16)
+    assert status_of(B.hc_reduce_scatter, s, rs_out, P, n, "float32", "sum", "ring", o) == SCR
+    o = B.make_opts("step", scratch=BASE + 256 * MB + 8, scratch_bytes=need + 64)
+    assert status_of(B.hc_reduce_scatter, s, rs_out, P, n, "float32", "sum", "ring", o) == ALN
+    # scratch overlapping a rank buffer
+    o = B.make_opts("step", scratch=s[1], scratch_bytes=need)
+    assert status_of(B.hc_reduce_scatter, s, rs_out, P, n, "float32", "sum", "ring", o) == INV
+    # count == 0 is a no-op success, even with no buffers
+    assert status_of(B.hc_allreduce, None, None, P, 0, "float32", "sum", "ring") == 0
+    # bad opts struct size
+    o = B.make_opts("fused")
+    o.struct_size = 8
+    assert status_of(B.hc_allreduce, s, d, P, n, "float32", "sum", "ring", o) == INV
+
+
+@host_only
+def test_valid_call_without_gpu_reports_cuda_error():
+    """Everything valid: the only failure left is the missing device."""
+    P, n = 4, 1024
+    st = status_of(B.hc_allreduce, fake(P), fake(P, base=BASE + 64 * MB), P, n, "float32", "sum", "ring")
+    assert st == 5
+
+
+def test_status_strings():
+    assert B.status_string(0) == "success"
+    assert "aligned" in B.status_string(3)
+    assert B.status_string(42) == "unknown status"
