@@ -116,18 +116,24 @@ hc_status_t run(hc_coll_t coll, const void* const* send, void* const* recv, int 
     if (count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
     if (!recv) return HC_ERR_INVALID_ARG;
     if (!send && coll != HC_COLL_ALLGATHER) return HC_ERR_INVALID_ARG;
-    for (int r = 0; r < P; r++) {
-        if (!recv[r] || (send && !send[r])) return HC_ERR_INVALID_ARG;
-    }
-    for (int r = 0; r < P; r++) {
-        if (((uintptr_t)recv[r] & 15) || (send && ((uintptr_t)send[r] & 15))) return HC_ERR_ALIGN;
-    }
 
     const int64_t n = (int64_t)count;
     const int es = elem_bytes(dtype);
     const Layout lay = make_layout(algo, coll, P, n, dtype);
     // for ReduceScatter / AllGather, the per-rank segment is the rank's own
     const Layout own = make_layout(algo, coll, P, n, dtype);
+
+    // a buffer of zero elements (the ReduceScatter output or AllGather input
+    // of an empty trailing segment) is never touched: it may be NULL or
+    // unaligned; every other buffer must be non-null and 16-byte aligned
+    for (int r = 0; r < P; r++) {
+        const bool seg_empty = own.seg_hi(r) == own.seg_lo(r);
+        const bool recv_used = !(coll == HC_COLL_REDUCE_SCATTER && seg_empty);
+        const bool send_used = send && !(coll == HC_COLL_ALLGATHER && seg_empty);
+        if ((recv_used && !recv[r]) || (send_used && !send[r])) return HC_ERR_INVALID_ARG;
+        if ((recv_used && ((uintptr_t)recv[r] & 15)) || (send_used && ((uintptr_t)send[r] & 15)))
+            return HC_ERR_ALIGN;
+    }
 
     Aliasing al;
     std::memset(&al, 0, sizeof al);
