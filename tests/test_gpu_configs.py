@@ -49,11 +49,12 @@ def sample(algo, coll, P, n, dtype, loop_bytes=0, p_intra=1, count=20000):
     return hc_inputs.sample_indices(n, count, seed=P + n, segment_edges=edges)
 
 
-def check_sampled(coll, algo, X, dtype, op, mode, p_intra=1, loop_bytes=0, in_place=False):
+def check_sampled(coll, algo, X, dtype, op, mode, p_intra=1, loop_bytes=0, in_place=False,
+                  count=20000):
     P, n = X.shape
     res, ok = run_collective(coll, algo, X, dtype, op, mode, in_place, p_intra, loop_bytes)
     assert ok
-    J = sample(algo, coll, P, n, dtype, loop_bytes, p_intra)
+    J = sample(algo, coll, P, n, dtype, loop_bytes, p_intra, count=count)
     Y = O.replay(algo, coll, X, op, dtype, p_intra=p_intra, loop_bytes=loop_bytes, J=J)
     segs = segments(algo, coll, P, n, dtype)
     for r in range(P):
