@@ -53,7 +53,8 @@ class hc_plan_record_t(ctypes.Structure):
 
 
 # every symbol include/hc.h declares
-EXPORTS = ("hc_allreduce", "hc_reduce_scatter", "hc_allgather", "hc_segment_range",
+EXPORTS = ("hc_allreduce", "hc_reduce_scatter", "hc_reduce_scatter_static_scratch",
+           "hc_allgather", "hc_segment_range",
            "hc_num_segments", "hc_scratch_bytes", "hc_schedule_stats", "hc_step_plan",
            "hc_status_string", "hc_version")
 
@@ -74,6 +75,9 @@ def lib():
             f = getattr(L, name)
             f.argtypes = [ptrs, ptrs, i32, sz, i32, i32, i32, ctypes.POINTER(hc_opts_t), vp]
             f.restype = i32
+        L.hc_reduce_scatter_static_scratch.argtypes = [ptrs, ptrs, i32, sz, i32, i32, i32, i32,
+                                                       sz, vp]
+        L.hc_reduce_scatter_static_scratch.restype = i32
         L.hc_allgather.argtypes = [ptrs, ptrs, i32, sz, i32, i32, ctypes.POINTER(hc_opts_t), vp]
         L.hc_allgather.restype = i32
         L.hc_segment_range.argtypes = [i32, i32, i32, sz, i32, i32,
@@ -149,6 +153,17 @@ def hc_reduce_scatter(send, recv, P, count, dtype, op, algo, opts=None, stream=0
                                  ctypes.byref(opts) if opts is not None else None,
                                  ctypes.c_void_p(int(stream)) if stream else None)
     _check(st, "hc_reduce_scatter")
+
+
+def hc_reduce_scatter_static_scratch(send, recv, P, count, dtype, op, algo, ranks_per_server=1,
+                                     max_loop_bytes=0, stream=0):
+    """Step-mode ReduceScatter whose working memory is the library's own
+    fixed device array (for callers that may not allocate device memory)."""
+    st = lib().hc_reduce_scatter_static_scratch(
+        _ptr_array(send), _ptr_array(recv), int(P), int(count), _enum(DTYPES, dtype),
+        _enum(OPS, op), _enum(ALGOS, algo), int(ranks_per_server), int(max_loop_bytes),
+        ctypes.c_void_p(int(stream)) if stream else None)
+    _check(st, "hc_reduce_scatter_static_scratch")
 
 
 def hc_allgather(send, recv, P, count, dtype, algo, opts=None, stream=0):

@@ -159,6 +159,38 @@ hc_status_t hc_reduce_scatter(const void* const* send, void* const* recv, int P,
                               const hc_opts_t* opts, hc_stream_t stream);
 
 /*
+ * ReduceScatter for callers that may not allocate device memory.  The pages
+ * have no counterpart to this entry point; it exists for callers such as a
+ * plugin that a host framework hands only its input and output buffers
+ * (the framework owns all device memory through its own pool), or a
+ * latency-critical path that cannot afford cudaMalloc's implicit
+ * synchronisation or its failure under memory pressure.
+ *
+ * It computes exactly what hc_reduce_scatter computes in step mode
+ * (HC_MODE_STEP, same arguments and buffer conventions, bit-identical
+ * results), but the working memory of out-of-place ranks is a fixed array of
+ * HC_STATIC_SCRATCH_BYTES that the library places in the memory of every GPU
+ * that loads it, held until the process exits.  It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *  - Work needing more than HC_STATIC_SCRATCH_BYTES (P * roundup(count * b,
+ *    256) bytes, see hc_scratch_bytes) is rejected with HC_ERR_SCRATCH before
+ *    anything is launched.
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps whatever the last call left
+ *    there; nothing in it needs to start at zero, because every location is
+ *    written before it is read within a call.  Calls that overlap on the GPU
+ *    (different streams, or different host threads) race on the array:
+ *    order them on one stream.
+ */
+#define HC_STATIC_SCRATCH_BYTES (32u << 20)
+hc_status_t hc_reduce_scatter_static_scratch(const void* const* send, void* const* recv, int P,
+                                             size_t count, hc_dtype_t dtype, hc_op_t op,
+                                             hc_algo_t algo, int ranks_per_server,
+                                             size_t max_loop_bytes, hc_stream_t stream);
+
+/*
  * AllGather: recv[r][off_k .. off_k + len_k) = send[k][0 .. len_k) for every
  * rank r and segment k.  (Ring: all-gather phase; RHD: Table 1 AllGather row;
  * Pipeline: "AllGather 算子的 Pipeline 时序编排", LocalCopy of "Rank0 视角".)
