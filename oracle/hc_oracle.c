@@ -45,6 +45,15 @@
  *   sym   : symbolic mode; every value is an expression-tree node, used to
  *           read off the association order each schedule implies.
  *
+ * Parity of the Pipeline ReduceScatter / AllReduce association order: the
+ * pages narrate only the Pipeline AllGather and call the other two
+ * "symmetric".  The order used here (a lone intra-server mesh reduce, then
+ * the inter-server chain starting at server s+1) is pinned by the definition,
+ * by every rank contributing exactly once and by Table 1's step structure,
+ * but no printed value fixes the floating-point order itself: for fp32/bf16
+ * sum and prod of the Pipeline ReduceScatter / AllReduce, parity unpinned
+ * beyond those checks.
+ *
  * Built with -O2 -ffp-contract=off and no fast-math (see build.py).
  */
 #include <stdint.h>
