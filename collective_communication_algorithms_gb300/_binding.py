@@ -56,7 +56,7 @@ class hc_plan_record_t(ctypes.Structure):
 EXPORTS = ("hc_allreduce", "hc_reduce_scatter", "hc_reduce_scatter_static_scratch",
            "hc_allgather", "hc_segment_range",
            "hc_num_segments", "hc_scratch_bytes", "hc_schedule_stats", "hc_step_plan",
-           "hc_status_string", "hc_version")
+           "hc_device_status", "hc_status_string", "hc_version")
 
 _lib = None
 
@@ -95,6 +95,8 @@ def lib():
                                    ctypes.POINTER(hc_plan_record_t), sz,
                                    ctypes.POINTER(sz), ctypes.POINTER(i32)]
         L.hc_step_plan.restype = i32
+        L.hc_device_status.argtypes = [i32]
+        L.hc_device_status.restype = i32
         L.hc_status_string.argtypes = [i32]
         L.hc_status_string.restype = ctypes.c_char_p
         L.hc_version.argtypes = []
@@ -224,6 +226,11 @@ def hc_step_plan(algo, coll, P, count, dtype, ranks_per_server=1, max_loop_bytes
                     "in_ranks": list(r.in_ranks[:r.in_cnt]),
                     "out_ranks": list(r.out_ranks[:r.out_cnt])})
     return out, nl.value
+
+
+def hc_device_status(clear=True):
+    """HC_OK (0) or HC_ERR_TIMEOUT (6) recorded by a bounded device-side wait."""
+    return lib().hc_device_status(1 if clear else 0)
 
 
 def hc_version():

@@ -376,6 +376,12 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
     return HC_OK;
 }
 
+hc_status_t hc_device_status(int clear) {
+    int v = 0;
+    if (read_device_error(clear != 0, &v) != cudaSuccess) return HC_ERR_CUDA;
+    return v ? (hc_status_t)v : HC_OK;
+}
+
 const char* hc_status_string(hc_status_t s) {
     switch (s) {
     case HC_OK: return "success";

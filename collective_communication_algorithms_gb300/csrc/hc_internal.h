@@ -137,6 +137,8 @@ struct FusedArgs {
 
 // Kernel launchers (hc_kernels.cu).
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count);
+// Reads (and optionally clears) the device-side error flag of the TMA kernels.
+cudaError_t read_device_error(bool clear, int* status);
 cudaError_t launch_step(const Plan& plan, int P, hc_dtype_t dt, hc_op_t op,
                         const uintptr_t (&base)[LOC_COUNT][kMaxRanks], cudaStream_t stream,
                         int sm_count);

@@ -202,11 +202,25 @@ struct FusedParams {
     int p_intra;
     int pp;                    // RHD: power-of-two core size
     int rfold;                 // RHD: number of folded pairs
+    int stages;                // TMA kernels: pipeline depth
     unsigned long long skip_mask;  // AllGather: ranks whose own segment is already in place
 };
 
 constexpr int kFusedThreads = 256;
 constexpr int kBatch = 8;
+
+// V 16-byte vectors handled together by one thread (more loads in flight)
+template <int V>
+struct VecN {
+    uint4 v[V];
+};
+template <hc_dtype_t DT, hc_op_t OP, int V>
+__device__ __forceinline__ VecN<V> vop(const VecN<V>& a, const VecN<V>& b) {
+    VecN<V> r;
+#pragma unroll
+    for (int j = 0; j < V; j++) r.v[j] = vop<DT, OP>(a.v[j], b.v[j]);
+    return r;
+}
 
 // Reduce a chain x_0 (+) x_1 (+) ... (+) x_{cnt-1}, x_i = load(rank(i)), with
 // loads issued kBatch at a time for memory-level parallelism.
@@ -298,8 +312,27 @@ __device__ __forceinline__ V segment_reduce(const FusedParams& p, int k, Load lo
     }
 }
 
-// AllReduce (COLL = 0) and ReduceScatter (COLL = 1).  grid.y = segment.
+// Ragged end of segment k: the fewer than A elements after its last full
+// vector, element by element (one thread).
 template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP>
+__device__ void ragged_tail(const FusedParams& p, int k, int64_t from, int64_t to) {
+    constexpr int ES = DT_<DT>::ES;
+    for (int64_t x = from; x < to; x++) {
+        const uintptr_t xo = (uintptr_t)x * ES;
+        auto load = [&](int r) -> uint32_t { return ld_elem<ES>(p.src[r] + xo); };
+        uint32_t acc = segment_reduce<ALGO, DT, OP, uint32_t>(p, k, load);
+        if (COLL == 0) {
+            for (int r = 0; r < p.P; r++) st_elem<ES>(p.dst[r] + xo, acc);
+        } else {
+            st_elem<ES>(p.dst[k] + xo, acc);
+        }
+    }
+}
+
+// AllReduce (COLL = 0) and ReduceScatter (COLL = 1), register path: every
+// thread loads V vectors of a segment from every rank straight into
+// registers.  grid.y = segment.
+template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP, int V>
 __global__ void __launch_bounds__(kFusedThreads)
 fused_reduce(const __grid_constant__ FusedParams p) {
     constexpr int ES = DT_<DT>::ES;
@@ -309,34 +342,36 @@ fused_reduce(const __grid_constant__ FusedParams p) {
     if (sbeg >= p.n) return;
     const int64_t send_ = (sbeg + p.L < p.n) ? sbeg + p.L : p.n;
     const int64_t nfull = (send_ - sbeg) / A;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nfull; v += stride) {
-        const uintptr_t off = (uintptr_t)(sbeg + v * A) * ES;
-        auto load = [&](int r) -> uint4 { return ld_stream(p.src[r] + off); };
-        uint4 acc = segment_reduce<ALGO, DT, OP, uint4>(p, k, load);
-        if (COLL == 0) {
-            for (int r = 0; r < p.P; r++) st_stream(p.dst[r] + off, acc);
-        } else {
-            st_stream(p.dst[k] + off, acc);
-        }
-    }
-    // ragged end: fewer than A elements after the last full vector
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        for (int64_t x = sbeg + nfull * A; x < send_; x++) {
-            const uintptr_t xo = (uintptr_t)x * ES;
-            auto load = [&](int r) -> uint32_t { return ld_elem<ES>(p.src[r] + xo); };
-            uint32_t acc = segment_reduce<ALGO, DT, OP, uint32_t>(p, k, load);
+    const int64_t chunk = (int64_t)V * blockDim.x;
+    for (int64_t base = (int64_t)blockIdx.x * chunk; base < nfull; base += (int64_t)gridDim.x * chunk) {
+        auto load = [&](int r) -> VecN<V> {
+            VecN<V> x;
+#pragma unroll
+            for (int j = 0; j < V; j++) {
+                const int64_t v = base + threadIdx.x + (int64_t)j * blockDim.x;
+                x.v[j] = v < nfull ? ld_stream(p.src[r] + (uintptr_t)(sbeg + v * A) * ES)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            }
+            return x;
+        };
+        const VecN<V> acc = segment_reduce<ALGO, DT, OP, VecN<V>>(p, k, load);
+#pragma unroll
+        for (int j = 0; j < V; j++) {
+            const int64_t v = base + threadIdx.x + (int64_t)j * blockDim.x;
+            if (v >= nfull) continue;
+            const uintptr_t off = (uintptr_t)(sbeg + v * A) * ES;
             if (COLL == 0) {
-                for (int r = 0; r < p.P; r++) st_elem<ES>(p.dst[r] + xo, acc);
+                for (int r = 0; r < p.P; r++) st_stream(p.dst[r] + off, acc.v[j]);
             } else {
-                st_elem<ES>(p.dst[k] + xo, acc);
+                st_stream(p.dst[k] + off, acc.v[j]);
             }
         }
     }
+    if (blockIdx.x == 0 && threadIdx.x == 0) ragged_tail<ALGO, COLL, DT, OP>(p, k, sbeg + nfull * A, send_);
 }
 
-// AllGather: segment k read once from its owner, written to every rank
-// (the owner's own copy only when it is not already in place).
+// AllGather, register path: segment k read once from its owner, written to
+// every rank (the owner's own copy only when it is not already in place).
 template <int ES>
 __global__ void __launch_bounds__(kFusedThreads)
 fused_allgather(const __grid_constant__ FusedParams p) {
@@ -365,32 +400,274 @@ fused_allgather(const __grid_constant__ FusedParams p) {
 }
 
 // ---------------------------------------------------------------------------
+// TMA-staged fused kernels.  One elected thread moves whole 16-byte-aligned
+// tiles between HBM and shared memory with the bulk-copy engine
+// (cp.async.bulk), completion tracked by mbarrier transaction counts; the
+// block reduces from shared memory and the result tile goes back to every
+// output with bulk stores.  Every wait on an mbarrier is bounded: after
+// kWaitLimitNs the block records HC_ERR_TIMEOUT in hc_device_error, waits
+// (again bounded) for its copies in flight and returns.
+// ---------------------------------------------------------------------------
+constexpr int kTmaTile = 4096;          // bytes per rank per stage (reduce kernels)
+constexpr int kTmaThreads = 256;
+constexpr int kTmaMaxSmem = 200 * 1024;  // dynamic shared memory budget per CTA
+constexpr int kAgTile = 8192;           // bytes per stage (AllGather kernel)
+constexpr int kAgStages = 8;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ int hc_device_error;
+
+__device__ __forceinline__ unsigned smem_addr(const void* p) {
+    return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* m, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(m)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* m, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(m)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* m, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(m)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Poll an mbarrier phase for at most kWaitLimitNs.
+__device__ bool mbar_wait_bounded(uint64_t* m, unsigned parity) {
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(m, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, uintptr_t gsrc, unsigned bytes, uint64_t* m) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_addr(m))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(uintptr_t gdst, const void* smem_src, unsigned bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_addr(smem_src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// AllReduce (COLL = 0) / ReduceScatter (COLL = 1), TMA-staged.  grid.y =
+// segment; block x takes the segment's 4 KB tiles x, x + gridDim.x, ...
+// (concurrent blocks spread over all segments, which keeps DRAM pages open).
+// Shared memory: stages x P tiles of inputs, 2 output tiles, stage barriers.
+template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+fused_reduce_tma(const __grid_constant__ FusedParams p) {
+    constexpr int ES = DT_<DT>::ES;
+    constexpr int A = DT_<DT>::A;
+    extern __shared__ __align__(128) unsigned char smem[];
+    __shared__ int abort_flag;
+    const int P = p.P, D = p.stages, k = blockIdx.y;
+    unsigned char* in = smem;
+    unsigned char* out = in + (size_t)D * P * kTmaTile;
+    uint64_t* full = (uint64_t*)(out + 2 * kTmaTile);
+    const int64_t sbeg = (int64_t)k * p.L;
+    const int64_t send_ = sbeg + p.L < p.n ? sbeg + p.L : p.n;
+    const int64_t nfull = send_ > sbeg ? (send_ - sbeg) / A : 0;
+    const int64_t nbytes = nfull * 16;                        // tiled part of the segment
+    const uintptr_t seg_off = (uintptr_t)sbeg * ES;
+    const int64_t ntiles = (nbytes + kTmaTile - 1) / kTmaTile;
+    const int64_t first = blockIdx.x, step = gridDim.x;
+    const int64_t mine = first < ntiles ? (ntiles - first + step - 1) / step : 0;
+    auto tile_bytes = [&](int64_t t) -> unsigned {
+        const int64_t b = nbytes - t * kTmaTile;
+        return (unsigned)(b < kTmaTile ? b : kTmaTile);
+    };
+    auto issue_loads = [&](int s, int64_t t) {
+        const unsigned tb = tile_bytes(t);
+        mbar_arrive_expect_tx(&full[s], tb * (unsigned)P);
+        for (int r = 0; r < P; r++)
+            bulk_g2s(in + ((size_t)s * P + r) * kTmaTile, p.src[r] + seg_off + (uintptr_t)t * kTmaTile, tb,
+                     &full[s]);
+    };
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        for (int s = 0; s < D; s++) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int s = 0; s < D && s < mine; s++) issue_loads(s, first + s * step);
+    }
+    __syncthreads();
+    int64_t i = 0;
+    for (; i < mine; i++) {
+        const int s = (int)(i % D);
+        if (threadIdx.x == 0) {
+            if (!mbar_wait_bounded(&full[s], (unsigned)((i / D) & 1))) abort_flag = 1;
+            bulk_wait_read_1();  // output tile i & 1 no longer read by the stores of tile i - 2
+        }
+        __syncthreads();
+        if (abort_flag) break;
+        const int64_t t = first + i * step;
+        const unsigned tb = tile_bytes(t);
+        const unsigned char* st = in + (size_t)s * P * kTmaTile;
+        unsigned char* ob = out + (size_t)(i & 1) * kTmaTile;
+        for (unsigned v = threadIdx.x; v < tb / 16; v += blockDim.x) {
+            auto load = [&](int r) -> uint4 { return *(const uint4*)(st + (size_t)r * kTmaTile + v * 16); };
+            *(uint4*)(ob + v * 16) = segment_reduce<ALGO, DT, OP, uint4>(p, k, load);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            const uintptr_t off = seg_off + (uintptr_t)t * kTmaTile;
+            if (COLL == 0) {
+                for (int q = 0; q < P; q++) bulk_s2g(p.dst[q] + off, ob, tb);
+            } else {
+                bulk_s2g(p.dst[k] + off, ob, tb);
+            }
+            bulk_commit();
+            if (i + D < mine) issue_loads(s, first + (i + D) * step);
+        }
+    }
+    if (threadIdx.x == 0) {
+        bulk_wait_all();
+        if (abort_flag) {
+            atomicExch(&hc_device_error, (int)HC_ERR_TIMEOUT);
+            for (int64_t j = i; j < mine && j < i + D; j++)
+                mbar_wait_bounded(&full[j % D], (unsigned)((j / D) & 1));
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0 && !abort_flag)
+        ragged_tail<ALGO, COLL, DT, OP>(p, k, sbeg + nfull * A, send_);
+}
+
+// AllGather, TMA-staged: one thread streams the owner's segment through
+// shared memory in 8 KB tiles, each tile loaded once and bulk-stored to every
+// rank (the owner's own copy only when it is not already in place).
+template <int ES>
+__global__ void __launch_bounds__(32)
+fused_allgather_tma(const __grid_constant__ FusedParams p) {
+    constexpr int A = 16 / ES;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int k = blockIdx.y;
+    const int64_t sbeg = (int64_t)k * p.L;
+    const int64_t send_ = sbeg + p.L < p.n ? sbeg + p.L : p.n;
+    const int64_t nfull = send_ > sbeg ? (send_ - sbeg) / A : 0;
+    const bool skip_own = (p.skip_mask >> k) & 1ull;
+    if (threadIdx.x == 0) {
+        uint64_t* full = (uint64_t*)(smem + (size_t)kAgStages * kAgTile);
+        const int64_t nbytes = nfull * 16;
+        const uintptr_t seg_off = (uintptr_t)sbeg * ES;
+        const int64_t ntiles = (nbytes + kAgTile - 1) / kAgTile;
+        const int64_t first = blockIdx.x, step = gridDim.x;
+        const int64_t mine = first < ntiles ? (ntiles - first + step - 1) / step : 0;
+        auto tile_bytes = [&](int64_t t) -> unsigned {
+            const int64_t b = nbytes - t * kAgTile;
+            return (unsigned)(b < kAgTile ? b : kAgTile);
+        };
+        auto issue_load = [&](int s, int64_t t) {
+            const unsigned tb = tile_bytes(t);
+            mbar_arrive_expect_tx(&full[s], tb);
+            bulk_g2s(smem + (size_t)s * kAgTile, p.src[k] + seg_off + (uintptr_t)t * kAgTile, tb, &full[s]);
+        };
+        for (int s = 0; s < kAgStages; s++) mbar_init(&full[s], 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        for (int s = 0; s < kAgStages && s < mine; s++) issue_load(s, first + s * step);
+        bool aborted = false;
+        int64_t i = 0;
+        for (; i < mine; i++) {
+            const int s = (int)(i % kAgStages);
+            if (!mbar_wait_bounded(&full[s], (unsigned)((i / kAgStages) & 1))) {
+                aborted = true;
+                break;
+            }
+            const int64_t t = first + i * step;
+            const unsigned tb = tile_bytes(t);
+            const uintptr_t off = seg_off + (uintptr_t)t * kAgTile;
+            for (int r = 0; r < p.P; r++)
+                if (r != k || !skip_own) bulk_s2g(p.dst[r] + off, smem + (size_t)s * kAgTile, tb);
+            bulk_commit();
+            if (i >= 1) {
+                // the stores of tile i - 1 have read their stage: refill it
+                bulk_wait_read_1();
+                const int64_t nx = i - 1 + kAgStages;
+                if (nx < mine) issue_load((int)((i - 1) % kAgStages), first + nx * step);
+            }
+        }
+        bulk_wait_all();
+        if (aborted) {
+            atomicExch(&hc_device_error, (int)HC_ERR_TIMEOUT);
+            for (int64_t j = i; j < mine && j < i + kAgStages; j++)
+                mbar_wait_bounded(&full[j % kAgStages], (unsigned)((j / kAgStages) & 1));
+        } else if (blockIdx.x == 0) {
+            for (int64_t x = sbeg + nfull * A; x < send_; x++) {
+                const uintptr_t xo = (uintptr_t)x * ES;
+                const uint32_t val = ld_elem<ES>(p.src[k] + xo);
+                for (int r = 0; r < p.P; r++)
+                    if (r != k || !skip_own) st_elem<ES>(p.dst[r] + xo, val);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
 // dispatch
 // ---------------------------------------------------------------------------
+// kind: 1 / 2 = register path with 1 / 2 vectors per thread, 3 = TMA path
+template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP>
+void* pick_reduce_kind(int kind) {
+    if (kind == 3) return (void*)fused_reduce_tma<ALGO, COLL, DT, OP>;
+    if (kind == 2) return (void*)fused_reduce<ALGO, COLL, DT, OP, 2>;
+    return (void*)fused_reduce<ALGO, COLL, DT, OP, 1>;
+}
 template <hc_algo_t ALGO, int COLL, hc_dtype_t DT>
-void* pick_reduce_op(hc_op_t op) {
+void* pick_reduce_op(hc_op_t op, int kind) {
     switch (op) {
-    case HC_SUM: return (void*)fused_reduce<ALGO, COLL, DT, HC_SUM>;
-    case HC_PROD: return (void*)fused_reduce<ALGO, COLL, DT, HC_PROD>;
-    case HC_MAX: return (void*)fused_reduce<ALGO, COLL, DT, HC_MAX>;
-    default: return (void*)fused_reduce<ALGO, COLL, DT, HC_MIN>;
+    case HC_SUM: return pick_reduce_kind<ALGO, COLL, DT, HC_SUM>(kind);
+    case HC_PROD: return pick_reduce_kind<ALGO, COLL, DT, HC_PROD>(kind);
+    case HC_MAX: return pick_reduce_kind<ALGO, COLL, DT, HC_MAX>(kind);
+    default: return pick_reduce_kind<ALGO, COLL, DT, HC_MIN>(kind);
     }
 }
 template <hc_algo_t ALGO, int COLL>
-void* pick_reduce_dt(hc_dtype_t dt, hc_op_t op) {
+void* pick_reduce_dt(hc_dtype_t dt, hc_op_t op, int kind) {
     switch (dt) {
-    case HC_INT32: return pick_reduce_op<ALGO, COLL, HC_INT32>(op);
-    case HC_FLOAT32: return pick_reduce_op<ALGO, COLL, HC_FLOAT32>(op);
-    default: return pick_reduce_op<ALGO, COLL, HC_BFLOAT16>(op);
+    case HC_INT32: return pick_reduce_op<ALGO, COLL, HC_INT32>(op, kind);
+    case HC_FLOAT32: return pick_reduce_op<ALGO, COLL, HC_FLOAT32>(op, kind);
+    default: return pick_reduce_op<ALGO, COLL, HC_BFLOAT16>(op, kind);
     }
 }
 template <int COLL>
-void* pick_reduce(hc_algo_t algo, hc_dtype_t dt, hc_op_t op) {
+void* pick_reduce(hc_algo_t algo, hc_dtype_t dt, hc_op_t op, int kind) {
     switch (algo) {
-    case HC_ALGO_RING: return pick_reduce_dt<HC_ALGO_RING, COLL>(dt, op);
-    case HC_ALGO_RHD: return pick_reduce_dt<HC_ALGO_RHD, COLL>(dt, op);
-    default: return pick_reduce_dt<HC_ALGO_PIPELINE, COLL>(dt, op);
+    case HC_ALGO_RING: return pick_reduce_dt<HC_ALGO_RING, COLL>(dt, op, kind);
+    case HC_ALGO_RHD: return pick_reduce_dt<HC_ALGO_RHD, COLL>(dt, op, kind);
+    default: return pick_reduce_dt<HC_ALGO_PIPELINE, COLL>(dt, op, kind);
     }
+}
+
+// Raise a kernel's dynamic shared memory limit once.
+bool allow_smem(void* fn, int bytes) {
+    static void* done[512];
+    static int ndone = 0;
+    for (int i = 0; i < ndone; i++)
+        if (done[i] == fn) return true;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+        return false;
+    if (ndone < 512) done[ndone++] = fn;
+    return true;
 }
 
 template <int MAXI, hc_dtype_t DT>
@@ -491,26 +768,64 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     while (pp * 2 <= a.P) pp *= 2;
     p.pp = pp;
     p.rfold = a.P - pp;
-    int S = lay.S;
-    if (a.algo == HC_ALGO_RHD && a.coll == HC_COLL_ALLREDUCE) {
-        // the RHD tree is the same for every element: spread over P segments of
-        // the p'-segment layout (the grid only needs the element range)
-        S = lay.S;
-    }
-    const int64_t vecs_per_seg = (lay.L + lay.A - 1) / lay.A;
-    const int64_t want = std::max<int64_t>(1, (vecs_per_seg + kFusedThreads - 1) / kFusedThreads);
-    const int64_t cap = std::max<int64_t>(1, (int64_t)sm_count * (2048 / kFusedThreads) / S);
-    const int gx = (int)std::min(want, cap);
-    void* fn;
-    if (a.coll == HC_COLL_ALLGATHER) {
-        fn = es == 2 ? (void*)fused_allgather<2> : (void*)fused_allgather<4>;
-    } else if (a.coll == HC_COLL_ALLREDUCE) {
-        fn = pick_reduce<0>(a.algo, a.dtype, a.op);
-    } else {
-        fn = pick_reduce<1>(a.algo, a.dtype, a.op);
-    }
+    const int S = lay.S;
+    const int64_t seg_bytes = lay.L * es;
     void* args[] = {&p};
+
+    if (a.coll == HC_COLL_ALLGATHER) {
+        // TMA path once every segment holds several tiles per block
+        if (seg_bytes >= 16 * (int64_t)kAgTile) {
+            void* fn = es == 2 ? (void*)fused_allgather_tma<2> : (void*)fused_allgather_tma<4>;
+            const int smem = kAgStages * kAgTile + kAgStages * 8;
+            if (!allow_smem(fn, smem)) return cudaErrorInvalidValue;
+            int per_sm = 0;
+            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 32, smem);
+            if (e != cudaSuccess) return e;
+            const int64_t tiles = (seg_bytes + kAgTile - 1) / kAgTile;
+            const int gx = (int)std::max<int64_t>(
+                1, std::min<int64_t>(tiles, (int64_t)sm_count * std::max(1, per_sm) / S));
+            return cudaLaunchKernel(fn, dim3(gx, S), dim3(32), args, smem, stream);
+        }
+        void* fn = es == 2 ? (void*)fused_allgather<2> : (void*)fused_allgather<4>;
+        const int64_t vecs = (lay.L + lay.A - 1) / lay.A;
+        const int64_t want = std::max<int64_t>(1, (vecs + kFusedThreads - 1) / kFusedThreads);
+        const int gx = (int)std::min(want, std::max<int64_t>(1, (int64_t)sm_count * 4 / S));
+        return cudaLaunchKernel(fn, dim3(gx, S), dim3(kFusedThreads), args, 0, stream);
+    }
+
+    const int COLL = a.coll == HC_COLL_ALLREDUCE ? 0 : 1;
+    // TMA path: at most 8 ranks (so that 5 stages of P 4 KB tiles fit), and
+    // segments of at least 16 tiles
+    const int stages = (kTmaMaxSmem - 2 * kTmaTile - 64) / (a.P * kTmaTile);
+    if (a.P <= 8 && stages >= 2 && seg_bytes >= 16 * (int64_t)kTmaTile) {
+        p.stages = std::min(stages, 5);
+        void* fn = COLL == 0 ? pick_reduce<0>(a.algo, a.dtype, a.op, 3) : pick_reduce<1>(a.algo, a.dtype, a.op, 3);
+        const int smem = p.stages * a.P * kTmaTile + 2 * kTmaTile + p.stages * 8;
+        if (!allow_smem(fn, smem)) return cudaErrorInvalidValue;
+        const int64_t tiles = (seg_bytes + kTmaTile - 1) / kTmaTile;
+        const int gx = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count / S));
+        return cudaLaunchKernel(fn, dim3(gx, S), dim3(kTmaThreads), args, smem, stream);
+    }
+    // register path: 4 blocks of 256 threads per SM; two vectors per thread
+    // up to 16 ranks
+    const int V = a.P <= 16 ? 2 : 1;
+    void* fn = COLL == 0 ? pick_reduce<0>(a.algo, a.dtype, a.op, V) : pick_reduce<1>(a.algo, a.dtype, a.op, V);
+    const int64_t vecs = (lay.L + lay.A - 1) / lay.A;
+    const int64_t want = std::max<int64_t>(1, (vecs + (int64_t)V * kFusedThreads - 1) / ((int64_t)V * kFusedThreads));
+    const int gx = (int)std::min(want, std::max<int64_t>(1, (int64_t)sm_count * 4 / S));
     return cudaLaunchKernel(fn, dim3(gx, S), dim3(kFusedThreads), args, 0, stream);
+}
+
+cudaError_t read_device_error(bool clear, int* status) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, hc_device_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    *status = v;
+    if (clear && v) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(hc_device_error, &zero, sizeof(int));
+    }
+    return e;
 }
 
 }  // namespace hc

@@ -86,7 +86,7 @@ typedef enum {
     HC_ERR_ALIGN = 3,         /* a device pointer is not 16-byte aligned */
     HC_ERR_SCRATCH = 4,       /* step-mode scratch missing or too small */
     HC_ERR_CUDA = 5,          /* a CUDA launch or query failed */
-    HC_ERR_TIMEOUT = 6        /* reserved: a bounded device-side wait gave up */
+    HC_ERR_TIMEOUT = 6        /* a bounded device-side wait gave up (see hc_device_status) */
 } hc_status_t;
 
 typedef enum { HC_INT32 = 0, HC_FLOAT32 = 1, HC_BFLOAT16 = 2 } hc_dtype_t;
@@ -267,6 +267,16 @@ typedef struct {
 hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_server,
                          size_t count, hc_dtype_t dtype, size_t max_loop_bytes, int in_place,
                          hc_plan_record_t* records, size_t cap, size_t* n, int* launches);
+
+/*
+ * Device-side status of the kernels that wait on shared-memory barriers (the
+ * TMA-staged fused kernels).  Each such wait gives up after about 2 s; the
+ * kernel then records HC_ERR_TIMEOUT here and returns instead of hanging.
+ * Returns HC_OK, HC_ERR_TIMEOUT, or HC_ERR_CUDA if the flag cannot be read.
+ * Synchronises with the current device (it copies the flag to the host);
+ * clear != 0 resets the flag.
+ */
+hc_status_t hc_device_status(int clear);
 
 const char* hc_status_string(hc_status_t status);
 int hc_version(void);

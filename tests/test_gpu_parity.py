@@ -169,3 +169,31 @@ def test_uses_the_given_stream():
     assert ok
     Y = O.replay("ring", "allreduce", X, "sum", "float32")
     assert same_bits(res[0], Y[0], "float32")
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_tma_staged_paths(algo, dtype):
+    """Segments long enough for the TMA-staged fused kernels (at least 16
+    tiles of 4 KB per rank for AllReduce / ReduceScatter, 16 tiles of 8 KB for
+    AllGather), with a partial last tile and a ragged end."""
+    from collective_communication_algorithms_gb300 import _binding as B
+    per_seg = 40000 if dtype != "bfloat16" else 70000
+    for P in (2, 3, 5, 8):
+        pin = intra_for(algo, P) if algo != "pipeline" else (2 if P % 2 == 0 else 1)
+        n = P * per_seg + 13
+        for op in ("sum", "max"):
+            X = inputs(dtype, P, n, seed=P + 101, op=op)
+            for in_place in (False, True):
+                check("allreduce", algo, X, dtype, op, "fused", in_place, pin)
+                check("reducescatter", algo, X, dtype, op, "fused", in_place, pin)
+        X = inputs(dtype, P, 2 * n, seed=P + 202, op="sum")
+        for in_place in (False, True):
+            check("allgather", algo, X, dtype, "sum", "fused", in_place, pin)
+    assert B.hc_device_status() == 0
+
+
+def test_zz_no_device_timeouts_recorded():
+    """No bounded device-side wait gave up during the GPU tests above."""
+    from collective_communication_algorithms_gb300 import _binding as B
+    assert B.hc_device_status(clear=False) == 0
