@@ -26,7 +26,13 @@ class HcError(RuntimeError):
     def __init__(self, status, where):
         self.status = status
         self.name = STATUS.get(status, str(status))
-        super().__init__("%s: %s (%s)" % (where, self.name, status_string(status)))
+        detail = status_string(status)
+        if status == 5:
+            try:
+                detail += ", " + lib().hc_last_cuda_error().decode()
+            except Exception:
+                pass
+        super().__init__("%s: %s (%s)" % (where, self.name, detail))
 
 
 class hc_opts_t(ctypes.Structure):
@@ -56,7 +62,7 @@ class hc_plan_record_t(ctypes.Structure):
 EXPORTS = ("hc_allreduce", "hc_reduce_scatter", "hc_reduce_scatter_static_scratch",
            "hc_allgather", "hc_segment_range",
            "hc_num_segments", "hc_scratch_bytes", "hc_schedule_stats", "hc_step_plan",
-           "hc_device_status", "hc_status_string", "hc_version")
+           "hc_device_status", "hc_last_cuda_error", "hc_status_string", "hc_version")
 
 _lib = None
 
@@ -95,6 +101,8 @@ def lib():
                                    ctypes.POINTER(hc_plan_record_t), sz,
                                    ctypes.POINTER(sz), ctypes.POINTER(i32)]
         L.hc_step_plan.restype = i32
+        L.hc_last_cuda_error.argtypes = []
+        L.hc_last_cuda_error.restype = ctypes.c_char_p
         L.hc_device_status.argtypes = [i32]
         L.hc_device_status.restype = i32
         L.hc_status_string.argtypes = [i32]

@@ -63,6 +63,15 @@ bool any_overlap(std::vector<Interval> v) {
     return false;
 }
 
+// The CUDA error behind the last HC_ERR_CUDA returned on this thread.
+thread_local cudaError_t g_last_cuda_error = cudaSuccess;
+
+hc_status_t cuda_status(cudaError_t e) {
+    if (e == cudaSuccess) return HC_OK;
+    g_last_cuda_error = e;
+    return HC_ERR_CUDA;
+}
+
 int sm_count_of_current_device() {
     static int cache[64] = {0};
     int dev = 0;
@@ -185,7 +194,7 @@ hc_status_t run(hc_coll_t coll, const void* const* send, void* const* recv, int 
     if (any_overlap(iv)) return HC_ERR_INVALID_ARG;
 
     const int sms = sm_count_of_current_device();
-    if (sms <= 0) return HC_ERR_CUDA;
+    if (sms <= 0) return cuda_status(cudaErrorNoDevice);
 
     if (o.mode == HC_MODE_FUSED) {
         FusedArgs a;
@@ -201,8 +210,7 @@ hc_status_t run(hc_coll_t coll, const void* const* send, void* const* recv, int 
         a.recv = recv;
         std::memcpy(a.ag_in_place, ag_in_place, sizeof ag_in_place);
         std::memcpy(a.rs_in_place, rs_in_place, sizeof rs_in_place);
-        cudaError_t e = launch_fused(a, stream, sms);
-        return e == cudaSuccess ? HC_OK : HC_ERR_CUDA;
+        return cuda_status(launch_fused(a, stream, sms));
     }
 
     const Plan* plan = get_plan(algo, coll, P, o.p_intra, n, dtype, o.loop_bytes, al);
@@ -230,8 +238,7 @@ hc_status_t run(hc_coll_t coll, const void* const* send, void* const* recv, int 
             base[LOC_FINAL][r] = d;
         }
     }
-    cudaError_t e = launch_step(*plan, P, dtype, op, base, stream, sms);
-    return e == cudaSuccess ? HC_OK : HC_ERR_CUDA;
+    return cuda_status(launch_step(*plan, P, dtype, op, base, stream, sms));
 }
 
 }  // namespace
@@ -378,8 +385,13 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
 
 hc_status_t hc_device_status(int clear) {
     int v = 0;
-    if (read_device_error(clear != 0, &v) != cudaSuccess) return HC_ERR_CUDA;
+    const hc_status_t st = cuda_status(read_device_error(clear != 0, &v));
+    if (st != HC_OK) return st;
     return v ? (hc_status_t)v : HC_OK;
+}
+
+const char* hc_last_cuda_error(void) {
+    return g_last_cuda_error == cudaSuccess ? "cudaSuccess" : cudaGetErrorName(g_last_cuda_error);
 }
 
 const char* hc_status_string(hc_status_t s) {

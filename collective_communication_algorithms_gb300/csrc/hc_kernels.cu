@@ -400,18 +400,18 @@ fused_allgather(const __grid_constant__ FusedParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// TMA-staged fused kernels.  One elected thread moves whole 16-byte-aligned
-// tiles between HBM and shared memory with the bulk-copy engine
-// (cp.async.bulk), completion tracked by mbarrier transaction counts; the
-// block reduces from shared memory and the result tile goes back to every
-// output with bulk stores.  Every wait on an mbarrier is bounded: after
-// kWaitLimitNs the block records HC_ERR_TIMEOUT in hc_device_error, waits
-// (again bounded) for its copies in flight and returns.
+// TMA-staged AllGather.  One elected thread moves whole 16-byte-aligned tiles
+// between HBM and shared memory with the bulk-copy engine (cp.async.bulk),
+// completion tracked by mbarrier transaction counts, and bulk-stores every
+// tile from shared memory to all outputs.  Every wait on an mbarrier is
+// bounded: after kWaitLimitNs the block records HC_ERR_TIMEOUT in
+// hc_device_error, waits (again bounded) for its copies in flight and
+// returns.  (A TMA-staged reduce, one block per SM reducing from shared
+// memory, measured slower than the register path on GB300 for every
+// AllReduce / ReduceScatter shape tried: with 8 warps per SM the barrier
+// waits and the reduction could not hide behind the copies.)
 // ---------------------------------------------------------------------------
-constexpr int kTmaTile = 4096;          // bytes per rank per stage (reduce kernels)
-constexpr int kTmaThreads = 256;
-constexpr int kTmaMaxSmem = 200 * 1024;  // dynamic shared memory budget per CTA
-constexpr int kAgTile = 8192;           // bytes per stage (AllGather kernel)
+constexpr int kAgTile = 8192;           // bytes per stage
 constexpr int kAgStages = 8;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
@@ -468,89 +468,6 @@ __device__ __forceinline__ void bulk_wait_read_1() {
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// AllReduce (COLL = 0) / ReduceScatter (COLL = 1), TMA-staged.  grid.y =
-// segment; block x takes the segment's 4 KB tiles x, x + gridDim.x, ...
-// (concurrent blocks spread over all segments, which keeps DRAM pages open).
-// Shared memory: stages x P tiles of inputs, 2 output tiles, stage barriers.
-template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP>
-__global__ void __launch_bounds__(kTmaThreads, 1)
-fused_reduce_tma(const __grid_constant__ FusedParams p) {
-    constexpr int ES = DT_<DT>::ES;
-    constexpr int A = DT_<DT>::A;
-    extern __shared__ __align__(128) unsigned char smem[];
-    __shared__ int abort_flag;
-    const int P = p.P, D = p.stages, k = blockIdx.y;
-    unsigned char* in = smem;
-    unsigned char* out = in + (size_t)D * P * kTmaTile;
-    uint64_t* full = (uint64_t*)(out + 2 * kTmaTile);
-    const int64_t sbeg = (int64_t)k * p.L;
-    const int64_t send_ = sbeg + p.L < p.n ? sbeg + p.L : p.n;
-    const int64_t nfull = send_ > sbeg ? (send_ - sbeg) / A : 0;
-    const int64_t nbytes = nfull * 16;                        // tiled part of the segment
-    const uintptr_t seg_off = (uintptr_t)sbeg * ES;
-    const int64_t ntiles = (nbytes + kTmaTile - 1) / kTmaTile;
-    const int64_t first = blockIdx.x, step = gridDim.x;
-    const int64_t mine = first < ntiles ? (ntiles - first + step - 1) / step : 0;
-    auto tile_bytes = [&](int64_t t) -> unsigned {
-        const int64_t b = nbytes - t * kTmaTile;
-        return (unsigned)(b < kTmaTile ? b : kTmaTile);
-    };
-    auto issue_loads = [&](int s, int64_t t) {
-        const unsigned tb = tile_bytes(t);
-        mbar_arrive_expect_tx(&full[s], tb * (unsigned)P);
-        for (int r = 0; r < P; r++)
-            bulk_g2s(in + ((size_t)s * P + r) * kTmaTile, p.src[r] + seg_off + (uintptr_t)t * kTmaTile, tb,
-                     &full[s]);
-    };
-    if (threadIdx.x == 0) {
-        abort_flag = 0;
-        for (int s = 0; s < D; s++) mbar_init(&full[s], 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int s = 0; s < D && s < mine; s++) issue_loads(s, first + s * step);
-    }
-    __syncthreads();
-    int64_t i = 0;
-    for (; i < mine; i++) {
-        const int s = (int)(i % D);
-        if (threadIdx.x == 0) {
-            if (!mbar_wait_bounded(&full[s], (unsigned)((i / D) & 1))) abort_flag = 1;
-            bulk_wait_read_1();  // output tile i & 1 no longer read by the stores of tile i - 2
-        }
-        __syncthreads();
-        if (abort_flag) break;
-        const int64_t t = first + i * step;
-        const unsigned tb = tile_bytes(t);
-        const unsigned char* st = in + (size_t)s * P * kTmaTile;
-        unsigned char* ob = out + (size_t)(i & 1) * kTmaTile;
-        for (unsigned v = threadIdx.x; v < tb / 16; v += blockDim.x) {
-            auto load = [&](int r) -> uint4 { return *(const uint4*)(st + (size_t)r * kTmaTile + v * 16); };
-            *(uint4*)(ob + v * 16) = segment_reduce<ALGO, DT, OP, uint4>(p, k, load);
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            const uintptr_t off = seg_off + (uintptr_t)t * kTmaTile;
-            if (COLL == 0) {
-                for (int q = 0; q < P; q++) bulk_s2g(p.dst[q] + off, ob, tb);
-            } else {
-                bulk_s2g(p.dst[k] + off, ob, tb);
-            }
-            bulk_commit();
-            if (i + D < mine) issue_loads(s, first + (i + D) * step);
-        }
-    }
-    if (threadIdx.x == 0) {
-        bulk_wait_all();
-        if (abort_flag) {
-            atomicExch(&hc_device_error, (int)HC_ERR_TIMEOUT);
-            for (int64_t j = i; j < mine && j < i + D; j++)
-                mbar_wait_bounded(&full[j % D], (unsigned)((j / D) & 1));
-        }
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0 && !abort_flag)
-        ragged_tail<ALGO, COLL, DT, OP>(p, k, sbeg + nfull * A, send_);
 }
 
 // AllGather, TMA-staged: one thread streams the owner's segment through
@@ -625,10 +542,9 @@ fused_allgather_tma(const __grid_constant__ FusedParams p) {
 // ---------------------------------------------------------------------------
 // dispatch
 // ---------------------------------------------------------------------------
-// kind: 1 / 2 = register path with 1 / 2 vectors per thread, 3 = TMA path
+// kind: 1 / 2 vectors per thread
 template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP>
 void* pick_reduce_kind(int kind) {
-    if (kind == 3) return (void*)fused_reduce_tma<ALGO, COLL, DT, OP>;
     if (kind == 2) return (void*)fused_reduce<ALGO, COLL, DT, OP, 2>;
     return (void*)fused_reduce<ALGO, COLL, DT, OP, 1>;
 }
@@ -658,15 +574,19 @@ void* pick_reduce(hc_algo_t algo, hc_dtype_t dt, hc_op_t op, int kind) {
     }
 }
 
-// Raise a kernel's dynamic shared memory limit once.
+// Raise a kernel's dynamic shared memory limit to at least `bytes` (the
+// attribute is per kernel, so remember the largest value set for each).
 bool allow_smem(void* fn, int bytes) {
-    static void* done[512];
-    static int ndone = 0;
-    for (int i = 0; i < ndone; i++)
-        if (done[i] == fn) return true;
+    static void* fns[512];
+    static int set[512];
+    static int nfns = 0;
+    int i = 0;
+    while (i < nfns && fns[i] != fn) i++;
+    if (i < nfns && set[i] >= bytes) return true;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
         return false;
-    if (ndone < 512) done[ndone++] = fn;
+    if (i == nfns && nfns < 512) fns[nfns++] = fn;
+    if (i < nfns) set[i] = bytes;
     return true;
 }
 
@@ -794,25 +714,31 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     }
 
     const int COLL = a.coll == HC_COLL_ALLREDUCE ? 0 : 1;
-    // TMA path: at most 8 ranks (so that 5 stages of P 4 KB tiles fit), and
-    // segments of at least 16 tiles
-    const int stages = (kTmaMaxSmem - 2 * kTmaTile - 64) / (a.P * kTmaTile);
-    if (a.P <= 8 && stages >= 2 && seg_bytes >= 16 * (int64_t)kTmaTile) {
-        p.stages = std::min(stages, 5);
-        void* fn = COLL == 0 ? pick_reduce<0>(a.algo, a.dtype, a.op, 3) : pick_reduce<1>(a.algo, a.dtype, a.op, 3);
-        const int smem = p.stages * a.P * kTmaTile + 2 * kTmaTile + p.stages * 8;
-        if (!allow_smem(fn, smem)) return cudaErrorInvalidValue;
-        const int64_t tiles = (seg_bytes + kTmaTile - 1) / kTmaTile;
-        const int gx = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, sm_count / S));
-        return cudaLaunchKernel(fn, dim3(gx, S), dim3(kTmaThreads), args, smem, stream);
+    // Register path.  Launch shape (vectors per thread V, blocks of 256
+    // threads per SM) chosen from measurements on GB300 (fraction of the
+    // measured copy bandwidth, reproducible to 0.5 % across processes):
+    //  ReduceScatter, or more than 16 ranks        V1, 8 per SM (0.92 - 0.94)
+    //  AllReduce, 4-byte types                     V1, 6 per SM (0.95)
+    //  AllReduce, bf16 max / min                   V1, 6 per SM (0.87)
+    //  AllReduce, bf16 sum / prod, RHD             V2, 6 per SM (0.97)
+    //  AllReduce, bf16 sum / prod, Ring / Pipeline V1, 4 per SM (0.95)
+    int V = 1, per_sm = 8;
+    if (COLL == 0 && a.P <= 16) {
+        if (es == 4) {
+            per_sm = 6;
+        } else if (a.op == HC_MAX || a.op == HC_MIN) {
+            per_sm = 6;
+        } else if (a.algo == HC_ALGO_RHD) {
+            V = 2;
+            per_sm = 6;
+        } else {
+            per_sm = 4;
+        }
     }
-    // register path: 4 blocks of 256 threads per SM; two vectors per thread
-    // up to 16 ranks
-    const int V = a.P <= 16 ? 2 : 1;
     void* fn = COLL == 0 ? pick_reduce<0>(a.algo, a.dtype, a.op, V) : pick_reduce<1>(a.algo, a.dtype, a.op, V);
     const int64_t vecs = (lay.L + lay.A - 1) / lay.A;
     const int64_t want = std::max<int64_t>(1, (vecs + (int64_t)V * kFusedThreads - 1) / ((int64_t)V * kFusedThreads));
-    const int gx = (int)std::min(want, std::max<int64_t>(1, (int64_t)sm_count * 4 / S));
+    const int gx = (int)std::min(want, std::max<int64_t>(1, (int64_t)sm_count * per_sm / S));
     return cudaLaunchKernel(fn, dim3(gx, S), dim3(kFusedThreads), args, 0, stream);
 }
 

@@ -278,6 +278,10 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
  */
 hc_status_t hc_device_status(int clear);
 
+/* Name of the CUDA error (e.g. "cudaErrorInvalidValue") behind the last
+ * HC_ERR_CUDA this host thread received; "cudaSuccess" if none. */
+const char* hc_last_cuda_error(void);
+
 const char* hc_status_string(hc_status_t status);
 int hc_version(void);
 

@@ -174,9 +174,10 @@ def test_uses_the_given_stream():
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_tma_staged_paths(algo, dtype):
-    """Segments long enough for the TMA-staged fused kernels (at least 16
-    tiles of 4 KB per rank for AllReduce / ReduceScatter, 16 tiles of 8 KB for
-    AllGather), with a partial last tile and a ragged end."""
+    """Segments long enough for the TMA-staged AllGather (at least 16 tiles of
+    8 KB per segment), with a partial last tile and a ragged end; AllReduce and
+    ReduceScatter at the same sizes (register path with every launch shape the
+    library picks: 4- and 2-byte types, sum and max)."""
     from collective_communication_algorithms_gb300 import _binding as B
     per_seg = 40000 if dtype != "bfloat16" else 70000
     for P in (2, 3, 5, 8):
