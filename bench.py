@@ -91,6 +91,8 @@ def parse_args():
     ap.add_argument("--workload", default="ring_fp32_p8", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--sweep", choices=["small"], default=None,
+                    help="small: RHD AllReduce latency sweep (P x n), eager vs graph mode")
     return ap.parse_args()
 
 
@@ -477,8 +479,61 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
+def sweep_small(args):
+    """RHD AllReduce sum fp32, P in {5, 8, 12, 16}, n = 256 .. 16384: per-call
+    time eager (one host call per collective) and in graph mode (a graph of
+    `reps` dependent in-place AllReduces launched once), fused and step mode;
+    steps per call against ceil(log2 P).  Hot L2 (the data is tiny)."""
+    import math
+    import torch
+    from collective_communication_algorithms_gb300 import _binding as B
+    torch.cuda.set_device(0)
+    B.lib()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    reps = 200
+    for P in (5, 8, 12, 16):
+        for n in (256, 512, 1024, 2048, 4096, 8192, 16384):
+            X = hc_inputs.gradients_f32(P, n, seed=0, scale=1.0)
+            dev = torch.from_numpy(X).cuda()
+            ptrs = [dev[r].data_ptr() for r in range(P)]
+            st, _ = B.hc_schedule_stats("rhd", "allreduce", P, n, "float32")
+            line = {"sweep": "small", "algo": "rhd", "P": P, "elements_per_rank": n,
+                    "steps": st["steps_per_loop"], "ceil_log2_P": math.ceil(math.log2(P)),
+                    "launches_step": st["launches_step"]}
+            for mode in ("fused", "step"):
+                opts = B.make_opts(mode)
+                for _ in range(5):
+                    B.hc_allreduce(ptrs, ptrs, P, n, "float32", "sum", "rhd", opts, sh)
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(reps):
+                    B.hc_allreduce(ptrs, ptrs, P, n, "float32", "sum", "rhd", opts, sh)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                line["eager_%s_us" % mode] = round(e0.elapsed_time(e1) / reps * 1e3, 2)
+                g = B.Graph()
+                for _ in range(reps):
+                    g.add_allreduce(ptrs, ptrs, P, n, "float32", "sum", "rhd", opts)
+                g.build()
+                g.launch(sh)
+                torch.cuda.synchronize()
+                e0.record(stream)
+                g.launch(sh)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                line["graph_%s_us" % mode] = round(e0.elapsed_time(e1) / reps * 1e3, 2)
+                g.close()
+            print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
+    if args.sweep == "small":
+        sweep_small(args)
+        return
     if args.warmup < 3:
         args.warmup = 3
     w = WORKLOADS[args.workload]

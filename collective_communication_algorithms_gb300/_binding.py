@@ -60,7 +60,9 @@ class hc_plan_record_t(ctypes.Structure):
 
 # every symbol include/hc.h declares
 EXPORTS = ("hc_allreduce", "hc_reduce_scatter", "hc_reduce_scatter_static_scratch",
-           "hc_allgather", "hc_segment_range",
+           "hc_allgather", "hc_segment_range", "hc_graph_create", "hc_graph_add_allreduce",
+           "hc_graph_add_reduce_scatter", "hc_graph_add_allgather", "hc_graph_build",
+           "hc_graph_launch", "hc_graph_info", "hc_graph_destroy",
            "hc_num_segments", "hc_scratch_bytes", "hc_schedule_stats", "hc_step_plan",
            "hc_device_status", "hc_last_cuda_error", "hc_status_string", "hc_version")
 
@@ -86,6 +88,23 @@ def lib():
         L.hc_reduce_scatter_static_scratch.restype = i32
         L.hc_allgather.argtypes = [ptrs, ptrs, i32, sz, i32, i32, ctypes.POINTER(hc_opts_t), vp]
         L.hc_allgather.restype = i32
+        L.hc_graph_create.argtypes = [ctypes.POINTER(vp)]
+        L.hc_graph_create.restype = i32
+        for name in ("hc_graph_add_allreduce", "hc_graph_add_reduce_scatter"):
+            f = getattr(L, name)
+            f.argtypes = [vp, ptrs, ptrs, i32, sz, i32, i32, i32, ctypes.POINTER(hc_opts_t)]
+            f.restype = i32
+        L.hc_graph_add_allgather.argtypes = [vp, ptrs, ptrs, i32, sz, i32, i32,
+                                             ctypes.POINTER(hc_opts_t)]
+        L.hc_graph_add_allgather.restype = i32
+        for name in ("hc_graph_build", "hc_graph_destroy"):
+            getattr(L, name).argtypes = [vp]
+            getattr(L, name).restype = i32
+        L.hc_graph_launch.argtypes = [vp, vp]
+        L.hc_graph_launch.restype = i32
+        L.hc_graph_info.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32),
+                                    ctypes.POINTER(i32)]
+        L.hc_graph_info.restype = i32
         L.hc_segment_range.argtypes = [i32, i32, i32, sz, i32, i32,
                                        ctypes.POINTER(sz), ctypes.POINTER(sz)]
         L.hc_segment_range.restype = i32
@@ -239,6 +258,60 @@ def hc_step_plan(algo, coll, P, count, dtype, ranks_per_server=1, max_loop_bytes
 def hc_device_status(clear=True):
     """HC_OK (0) or HC_ERR_TIMEOUT (6) recorded by a bounded device-side wait."""
     return lib().hc_device_status(1 if clear else 0)
+
+
+class Graph:
+    """Graph mode: collectives added once, replayed with one launch."""
+
+    def __init__(self):
+        self.handle = ctypes.c_void_p()
+        _check(lib().hc_graph_create(ctypes.byref(self.handle)), "hc_graph_create")
+
+    def add_allreduce(self, send, recv, P, count, dtype, op, algo, opts=None):
+        _check(lib().hc_graph_add_allreduce(self.handle, _ptr_array(send), _ptr_array(recv),
+                                            int(P), int(count), _enum(DTYPES, dtype),
+                                            _enum(OPS, op), _enum(ALGOS, algo),
+                                            ctypes.byref(opts) if opts is not None else None),
+               "hc_graph_add_allreduce")
+
+    def add_reduce_scatter(self, send, recv, P, count, dtype, op, algo, opts=None):
+        _check(lib().hc_graph_add_reduce_scatter(self.handle, _ptr_array(send),
+                                                 _ptr_array(recv), int(P), int(count),
+                                                 _enum(DTYPES, dtype), _enum(OPS, op),
+                                                 _enum(ALGOS, algo),
+                                                 ctypes.byref(opts) if opts is not None else None),
+               "hc_graph_add_reduce_scatter")
+
+    def add_allgather(self, send, recv, P, count, dtype, algo, opts=None):
+        _check(lib().hc_graph_add_allgather(self.handle, _ptr_array(send), _ptr_array(recv),
+                                            int(P), int(count), _enum(DTYPES, dtype),
+                                            _enum(ALGOS, algo),
+                                            ctypes.byref(opts) if opts is not None else None),
+               "hc_graph_add_allgather")
+
+    def build(self):
+        _check(lib().hc_graph_build(self.handle), "hc_graph_build")
+
+    def launch(self, stream=0):
+        _check(lib().hc_graph_launch(self.handle, ctypes.c_void_p(int(stream)) if stream else None),
+               "hc_graph_launch")
+
+    def info(self):
+        a, b, c = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        _check(lib().hc_graph_info(self.handle, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)),
+               "hc_graph_info")
+        return {"collectives": a.value, "edges": b.value, "kernels": c.value}
+
+    def close(self):
+        if self.handle:
+            lib().hc_graph_destroy(self.handle)
+            self.handle = ctypes.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def hc_version():

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libhc.so")
 ARCHIVE = os.path.join(OUT, "libhc.a")
-SOURCES = ["hc_kernels.cu", "hc_sched.cpp", "hc_api.cpp", "hc_static_scratch.cu"]
+SOURCES = ["hc_kernels.cu", "hc_sched.cpp", "hc_api.cpp", "hc_graph.cpp", "hc_static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

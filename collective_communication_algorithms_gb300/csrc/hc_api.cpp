@@ -3,6 +3,7 @@
 #include <algorithm>
 #include <cstring>
 #include <map>
+#include <memory>
 #include <tuple>
 #include <vector>
 
@@ -46,10 +47,6 @@ hc_status_t read_opts(const hc_opts_t* o, hc_algo_t algo, int P, Opts* out) {
     return HC_OK;
 }
 
-struct Interval {
-    uintptr_t lo, hi;
-};
-
 // true when some two intervals overlap (empty intervals ignored)
 bool any_overlap(std::vector<Interval> v) {
     v.erase(std::remove_if(v.begin(), v.end(), [](const Interval& x) { return x.hi <= x.lo; }),
@@ -86,12 +83,12 @@ int sm_count_of_current_device() {
 // ---------------------------------------------------------------- plan cache
 using PlanKey = std::tuple<int, int, int, int, int64_t, int, int64_t, unsigned long long,
                            unsigned long long>;
-std::map<PlanKey, Plan>& plan_cache() {
-    static std::map<PlanKey, Plan> m;
+std::map<PlanKey, std::shared_ptr<const Plan>>& plan_cache() {
+    static std::map<PlanKey, std::shared_ptr<const Plan>> m;
     return m;
 }
 
-const Plan* get_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n,
+std::shared_ptr<const Plan> get_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n,
                      hc_dtype_t dt, int64_t loop_bytes, const Aliasing& al) {
     unsigned long long m1 = 0, m2 = 0;
     for (int r = 0; r < P; r++) {
@@ -101,11 +98,12 @@ const Plan* get_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t
     PlanKey key{(int)algo, (int)coll, P, p_intra, n, (int)dt, loop_bytes, m1, m2};
     auto& cache = plan_cache();
     auto it = cache.find(key);
-    if (it != cache.end()) return &it->second;
-    if (cache.size() >= 256) cache.clear();
-    Plan plan;
-    if (!build_plan(algo, coll, P, p_intra, n, dt, loop_bytes, al, &plan)) return nullptr;
-    return &cache.emplace(key, std::move(plan)).first->second;
+    if (it != cache.end()) return it->second;
+    if (cache.size() >= 256) cache.clear();  // plans still held by callers stay alive
+    auto plan = std::make_shared<Plan>();
+    if (!build_plan(algo, coll, P, p_intra, n, dt, loop_bytes, al, plan.get())) return nullptr;
+    cache.emplace(key, plan);
+    return plan;
 }
 
 size_t scratch_stride(size_t n, hc_dtype_t dt) {
@@ -113,24 +111,40 @@ size_t scratch_stride(size_t n, hc_dtype_t dt) {
     return (b + 255) / 256 * 256;
 }
 
-hc_status_t run(hc_coll_t coll, const void* const* send, void* const* recv, int P, size_t count,
-                hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts,
-                cudaStream_t stream) {
+}  // namespace
+
+namespace hc {
+
+// Validate one collective call and record everything its launch needs.
+hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, int P, size_t count,
+                    hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts,
+                    Prepared* out) {
+    *out = Prepared();
     if (!valid_dtype(dtype) || !valid_op(op) || !valid_algo(algo)) return HC_ERR_INVALID_ARG;
     if (P < 1 || P > kMaxRanks) return HC_ERR_INVALID_ARG;
     Opts o;
     hc_status_t st = read_opts(opts, algo, P, &o);
     if (st != HC_OK) return st;
-    if (count == 0) return HC_OK;
+    Prepared& c = *out;
+    c.coll = coll;
+    c.algo = algo;
+    c.dtype = dtype;
+    c.op = op;
+    c.P = P;
+    c.count = count;
+    c.mode = o.mode;
+    c.p_intra = o.p_intra;
+    c.loop_bytes = o.loop_bytes;
+    c.empty = count == 0;
+    if (c.empty) return HC_OK;
     if (count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
     if (!recv) return HC_ERR_INVALID_ARG;
     if (!send && coll != HC_COLL_ALLGATHER) return HC_ERR_INVALID_ARG;
 
     const int64_t n = (int64_t)count;
     const int es = elem_bytes(dtype);
-    const Layout lay = make_layout(algo, coll, P, n, dtype);
-    // for ReduceScatter / AllGather, the per-rank segment is the rank's own
-    const Layout own = make_layout(algo, coll, P, n, dtype);
+    c.lay = make_layout(algo, coll, P, n, dtype);
+    const Layout& own = c.lay;  // the per-rank segment of RS / AG is the rank's own
 
     // a buffer of zero elements (the ReduceScatter output or AllGather input
     // of an empty trailing segment) is never touched: it may be NULL or
@@ -144,45 +158,62 @@ hc_status_t run(hc_coll_t coll, const void* const* send, void* const* recv, int 
             return HC_ERR_ALIGN;
     }
 
-    Aliasing al;
-    std::memset(&al, 0, sizeof al);
-    bool rs_in_place[kMaxRanks] = {false}, ag_in_place[kMaxRanks] = {false};
+    std::memset(&c.al, 0, sizeof c.al);
     std::vector<Interval> iv;
     const uintptr_t full = (uintptr_t)n * es;
     for (int r = 0; r < P; r++) {
         const uintptr_t d = (uintptr_t)recv[r];
+        c.recv[r] = d;
         if (coll == HC_COLL_ALLREDUCE) {
             const uintptr_t s = (uintptr_t)send[r];
-            al.orig_is_work[r] = (s == d);
-            al.final_is_work[r] = true;
+            c.send[r] = s;
+            c.al.orig_is_work[r] = (s == d);
+            c.al.final_is_work[r] = true;
             iv.push_back({d, d + full});
-            if (s != d) iv.push_back({s, s + full});
+            c.writes.push_back({d, d + full});
+            if (s != d) {
+                iv.push_back({s, s + full});
+                c.reads.push_back({s, s + full});
+            }
         } else if (coll == HC_COLL_REDUCE_SCATTER) {
             const uintptr_t s = (uintptr_t)send[r];
+            c.send[r] = s;
             const uintptr_t off = (uintptr_t)own.seg_lo(r) * es;
             const uintptr_t len = (uintptr_t)(own.seg_hi(r) - own.seg_lo(r)) * es;
-            rs_in_place[r] = (d == s + off);
+            c.rs_in_place[r] = (d == s + off);
             iv.push_back({s, s + full});
-            if (!rs_in_place[r]) iv.push_back({d, d + len});
+            c.reads.push_back({s, s + full});
+            if (!c.rs_in_place[r]) {
+                iv.push_back({d, d + len});
+                c.writes.push_back({d, d + len});
+            } else {
+                c.writes.push_back({s, s + full});  // the input is working memory
+            }
         } else {
             const uintptr_t off = (uintptr_t)own.seg_lo(r) * es;
             const uintptr_t len = (uintptr_t)(own.seg_hi(r) - own.seg_lo(r)) * es;
             const uintptr_t s = send ? (uintptr_t)send[r] : d + off;
-            ag_in_place[r] = (s == d + off);
-            al.orig_is_work[r] = ag_in_place[r];
-            al.final_is_work[r] = true;
+            c.send[r] = s;
+            c.ag_in_place[r] = (s == d + off);
+            c.al.orig_is_work[r] = c.ag_in_place[r];
+            c.al.final_is_work[r] = true;
             iv.push_back({d, d + full});
-            if (!ag_in_place[r]) iv.push_back({s, s + len});
+            c.writes.push_back({d, d + full});
+            if (!c.ag_in_place[r]) {
+                iv.push_back({s, s + len});
+                c.reads.push_back({s, s + len});
+            }
         }
     }
+    c.has_send = send != nullptr;
 
     // step-mode ReduceScatter: working memory is the input (in place) or scratch
     bool need_scratch = false;
     if (coll == HC_COLL_REDUCE_SCATTER && o.mode == HC_MODE_STEP) {
         for (int r = 0; r < P; r++) {
-            al.orig_is_work[r] = rs_in_place[r];
-            al.final_is_work[r] = rs_in_place[r];
-            if (!rs_in_place[r]) need_scratch = true;
+            c.al.orig_is_work[r] = c.rs_in_place[r];
+            c.al.final_is_work[r] = c.rs_in_place[r];
+            if (!c.rs_in_place[r]) need_scratch = true;
         }
     }
     if (need_scratch) {
@@ -190,55 +221,89 @@ hc_status_t run(hc_coll_t coll, const void* const* send, void* const* recv, int 
         if (!o.scratch || o.scratch_bytes < need) return HC_ERR_SCRATCH;
         if ((uintptr_t)o.scratch & 15) return HC_ERR_ALIGN;
         iv.push_back({(uintptr_t)o.scratch, (uintptr_t)o.scratch + need});
+        c.writes.push_back({(uintptr_t)o.scratch, (uintptr_t)o.scratch + need});
+        c.scratch = (uintptr_t)o.scratch;
     }
     if (any_overlap(iv)) return HC_ERR_INVALID_ARG;
+    if (o.mode == HC_MODE_STEP) {
+        c.plan = get_plan(algo, coll, P, o.p_intra, n, dtype, o.loop_bytes, c.al);
+        if (!c.plan) return HC_ERR_INVALID_ARG;
+    }
+    return HC_OK;
+}
 
+// Launch a prepared call on a stream.
+hc_status_t execute(const Prepared& c, cudaStream_t stream) {
+    if (c.empty) return HC_OK;
     const int sms = sm_count_of_current_device();
     if (sms <= 0) return cuda_status(cudaErrorNoDevice);
-
-    if (o.mode == HC_MODE_FUSED) {
+    const int es = elem_bytes(c.dtype);
+    const Layout& own = c.lay;
+    if (c.mode == HC_MODE_FUSED) {
+        const void* sp[kMaxRanks];
+        void* rp[kMaxRanks];
+        for (int r = 0; r < c.P; r++) {
+            sp[r] = (const void*)c.send[r];
+            rp[r] = (void*)c.recv[r];
+        }
         FusedArgs a;
-        a.algo = algo;
-        a.coll = coll;
-        a.dtype = dtype;
-        a.op = op;
-        a.P = P;
-        a.p_intra = o.p_intra;
-        a.n = n;
-        a.lay = lay;
-        a.send = send;
-        a.recv = recv;
-        std::memcpy(a.ag_in_place, ag_in_place, sizeof ag_in_place);
-        std::memcpy(a.rs_in_place, rs_in_place, sizeof rs_in_place);
+        a.algo = c.algo;
+        a.coll = c.coll;
+        a.dtype = c.dtype;
+        a.op = c.op;
+        a.P = c.P;
+        a.p_intra = c.p_intra;
+        a.n = (int64_t)c.count;
+        a.lay = c.lay;
+        a.send = sp;
+        a.recv = rp;
+        std::memcpy(a.ag_in_place, c.ag_in_place, sizeof a.ag_in_place);
+        std::memcpy(a.rs_in_place, c.rs_in_place, sizeof a.rs_in_place);
         return cuda_status(launch_fused(a, stream, sms));
     }
-
-    const Plan* plan = get_plan(algo, coll, P, o.p_intra, n, dtype, o.loop_bytes, al);
-    if (!plan) return HC_ERR_INVALID_ARG;
     uintptr_t base[LOC_COUNT][kMaxRanks];
     std::memset(base, 0, sizeof base);
-    for (int r = 0; r < P; r++) {
-        const uintptr_t d = (uintptr_t)recv[r];
-        if (coll == HC_COLL_ALLREDUCE) {
-            base[LOC_ORIG][r] = (uintptr_t)send[r];
+    for (int r = 0; r < c.P; r++) {
+        const uintptr_t d = c.recv[r], s = c.send[r];
+        if (c.coll == HC_COLL_ALLREDUCE) {
+            base[LOC_ORIG][r] = s;
             base[LOC_WORK][r] = d;
             base[LOC_FINAL][r] = d;
-        } else if (coll == HC_COLL_REDUCE_SCATTER) {
-            const uintptr_t s = (uintptr_t)send[r];
+        } else if (c.coll == HC_COLL_REDUCE_SCATTER) {
             base[LOC_ORIG][r] = s;
-            base[LOC_WORK][r] = rs_in_place[r]
-                                    ? s
-                                    : (uintptr_t)o.scratch + (uintptr_t)r * scratch_stride(count, dtype);
+            base[LOC_WORK][r] = c.rs_in_place[r] ? s : c.scratch + (uintptr_t)r * scratch_stride(c.count, c.dtype);
             base[LOC_FINAL][r] = d - (uintptr_t)own.seg_lo(r) * es;
         } else {
             const uintptr_t off = (uintptr_t)own.seg_lo(r) * es;
-            const uintptr_t s = send ? (uintptr_t)send[r] : d + off;
             base[LOC_ORIG][r] = s - off;
             base[LOC_WORK][r] = d;
             base[LOC_FINAL][r] = d;
         }
     }
-    return cuda_status(launch_step(*plan, P, dtype, op, base, stream, sms));
+    return cuda_status(launch_step(*c.plan, c.P, c.dtype, c.op, base, stream, sms));
+}
+
+bool conflicts(const Prepared& a, const Prepared& b) {
+    auto hit = [](const std::vector<Interval>& x, const std::vector<Interval>& y) {
+        for (const Interval& i : x)
+            for (const Interval& j : y)
+                if (i.lo < j.hi && j.lo < i.hi && i.lo < i.hi && j.lo < j.hi) return true;
+        return false;
+    };
+    return hit(a.writes, b.writes) || hit(a.writes, b.reads) || hit(a.reads, b.writes);
+}
+
+}  // namespace hc
+
+namespace {
+
+hc_status_t run(hc_coll_t coll, const void* const* send, void* const* recv, int P, size_t count,
+                hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts,
+                cudaStream_t stream) {
+    Prepared c;
+    const hc_status_t st = prepare(coll, send, recv, P, count, dtype, op, algo, opts, &c);
+    if (st != HC_OK) return st;
+    return execute(c, stream);
 }
 
 }  // namespace

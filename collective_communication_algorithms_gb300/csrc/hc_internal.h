@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <memory>
 #include <vector>
 
 #include <cuda_runtime_api.h>
@@ -134,6 +135,44 @@ struct FusedArgs {
     bool ag_in_place[kMaxRanks];
     bool rs_in_place[kMaxRanks];
 };
+
+// ---------------------------------------------------------------------------
+// A validated collective call (hc_api.cpp): everything its launch needs, and
+// the device byte ranges it reads and writes (for graph dependencies).
+// ---------------------------------------------------------------------------
+struct Interval {
+    uintptr_t lo, hi;
+};
+
+struct Prepared {
+    hc_coll_t coll = HC_COLL_ALLREDUCE;
+    hc_algo_t algo = HC_ALGO_RING;
+    hc_dtype_t dtype = HC_FLOAT32;
+    hc_op_t op = HC_SUM;
+    hc_mode_t mode = HC_MODE_FUSED;
+    int P = 0;
+    int p_intra = 1;
+    int64_t loop_bytes = 0;
+    size_t count = 0;
+    bool empty = true;
+    bool has_send = false;
+    Layout lay;
+    Aliasing al;
+    bool rs_in_place[kMaxRanks] = {false};
+    bool ag_in_place[kMaxRanks] = {false};
+    uintptr_t send[kMaxRanks] = {0};
+    uintptr_t recv[kMaxRanks] = {0};
+    uintptr_t scratch = 0;
+    std::shared_ptr<const Plan> plan;  // step mode (shared with the plan cache)
+    std::vector<Interval> reads, writes;
+};
+
+hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, int P, size_t count,
+                    hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts,
+                    Prepared* out);
+hc_status_t execute(const Prepared& c, cudaStream_t stream);
+// true when b must wait for a (a write of one overlaps a read or write of the other)
+bool conflicts(const Prepared& a, const Prepared& b);
 
 // Kernel launchers (hc_kernels.cu).
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count);

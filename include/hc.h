@@ -203,6 +203,43 @@ hc_status_t hc_allgather(const void* const* send, void* const* recv, int P, size
                          hc_dtype_t dtype, hc_algo_t algo,
                          const hc_opts_t* opts, hc_stream_t stream);
 
+/*
+ * Graph mode ("Ascend950的AIV/AICPU通信引擎与图模式" of the Ring vs RHD
+ * article: HcclGraphAddAllReduce / HcclGraphBuild, whose build step analyses
+ * the data dependencies between collectives, orders them and emits one task
+ * list).  A graph is a list of collectives added once and replayed many
+ * times with one launch:
+ *  - hc_graph_add_* validate exactly like the eager entry points (same
+ *    arguments and buffer conventions) and record the call; the device
+ *    pointers and options are copied, the buffers must stay valid while the
+ *    graph is used.  Nothing is launched.
+ *  - Collective j depends on an earlier collective i when a device byte range
+ *    written by one is read or written by the other; independent collectives
+ *    may run concurrently.
+ *  - hc_graph_build captures every collective's kernels (on a private stream)
+ *    into one CUDA graph following those dependencies and instantiates it.
+ *    Adding a collective after a build discards the built graph.
+ *  - hc_graph_launch runs the built graph on `stream` (asynchronous); the
+ *    results equal running the collectives eagerly in the order added.
+ *  - hc_graph_info: collectives, dependency edges, kernel nodes (0 until built).
+ * A graph is not thread-safe; destroy it with hc_graph_destroy.
+ */
+typedef struct hc_graph_s* hc_graph_t;
+hc_status_t hc_graph_create(hc_graph_t* graph);
+hc_status_t hc_graph_add_allreduce(hc_graph_t graph, const void* const* send, void* const* recv,
+                                   int P, size_t count, hc_dtype_t dtype, hc_op_t op,
+                                   hc_algo_t algo, const hc_opts_t* opts);
+hc_status_t hc_graph_add_reduce_scatter(hc_graph_t graph, const void* const* send,
+                                        void* const* recv, int P, size_t count, hc_dtype_t dtype,
+                                        hc_op_t op, hc_algo_t algo, const hc_opts_t* opts);
+hc_status_t hc_graph_add_allgather(hc_graph_t graph, const void* const* send, void* const* recv,
+                                   int P, size_t count, hc_dtype_t dtype, hc_algo_t algo,
+                                   const hc_opts_t* opts);
+hc_status_t hc_graph_build(hc_graph_t graph);
+hc_status_t hc_graph_launch(hc_graph_t graph, hc_stream_t stream);
+hc_status_t hc_graph_info(hc_graph_t graph, int* collectives, int* edges, int* kernels);
+hc_status_t hc_graph_destroy(hc_graph_t graph);
+
 /* Segment k's element range (see the layout rule above).  k < S, where
  * S = hc_num_segments(algo, coll, P). */
 hc_status_t hc_segment_range(hc_algo_t algo, hc_coll_t coll, int P, size_t count,

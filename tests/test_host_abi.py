@@ -397,3 +397,36 @@ def test_status_strings():
     assert B.status_string(0) == "success"
     assert "aligned" in B.status_string(3)
     assert B.status_string(42) == "unknown status"
+
+
+@host_only
+def test_graph_dependency_analysis():
+    """Graph mode: collective j depends on an earlier i exactly when one writes
+    bytes the other reads or writes (fake pointers; nothing is launched)."""
+    P, n = 4, 1024
+    A = fake(P, base=BASE)
+    Bf = fake(P, base=BASE + 64 * MB)
+    C = fake(P, base=BASE + 128 * MB)
+    D = fake(P, base=BASE + 192 * MB)
+    g = B.Graph()
+    g.add_allreduce(A, A, P, n, "float32", "sum", "ring")           # 0: writes A
+    g.add_allreduce(C, C, P, n, "float32", "sum", "rhd")            # 1: independent
+    assert g.info() == {"collectives": 2, "edges": 0, "kernels": 0}
+    g.add_allreduce(A, Bf, P, n, "float32", "sum", "ring")          # 2: reads A -> after 0
+    assert g.info()["edges"] == 1
+    segs = [B.hc_segment_range("ring", "reducescatter", P, n, "float32", k) for k in range(P)]
+    rs_out = [D[r] + segs[r][0] * 4 for r in range(P)]
+    g.add_reduce_scatter(Bf, rs_out, P, n, "float32", "sum", "ring")  # 3: reads B (2), writes D
+    assert g.info()["edges"] == 2
+    g.add_allgather(rs_out, D, P, n, "float32", "ring")              # 4: in place on D -> after 3
+    assert g.info()["edges"] == 3
+    g.add_allreduce(C, Bf, P, n, "float32", "max", "ring")           # 5: reads C (1), writes B (2, 3)
+    info = g.info()
+    assert info["collectives"] == 6 and info["edges"] == 6
+    # an invalid collective is rejected at add time and not recorded
+    with pytest.raises(B.HcError):
+        g.add_allreduce(A, A, 0, n, "float32", "sum", "ring")
+    assert g.info()["collectives"] == 6
+    with pytest.raises(B.HcError):
+        g.launch()  # not built
+    g.close()
