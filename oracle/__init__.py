@@ -18,7 +18,7 @@ import numpy as np
 from . import build as _build
 
 ALGOS = {"ring": 0, "rhd": 1, "pipeline": 2}
-COLLS = {"allreduce": 0, "reducescatter": 1, "allgather": 2}
+COLLS = {"allreduce": 0, "reducescatter": 1, "allgather": 2, "broadcast": 3}
 DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
 NP_DTYPE = {"int32": np.int32, "float32": np.float32, "bfloat16": np.uint16}
@@ -59,15 +59,15 @@ def lib():
         L.orc_slicer.argtypes = [i32, i32, i32, i32, i64, i32, i64,
                                  ctypes.POINTER(i64), ctypes.POINTER(i32), ctypes.POINTER(i64)]
         L.orc_slicer.restype = i32
-        L.orc_schedule.argtypes = [i32, i32, i32, i32, i64, i32, i64,
+        L.orc_schedule.argtypes = [i32, i32, i32, i32, i32, i64, i32, i64,
                                    ctypes.POINTER(ctypes.POINTER(_Msg)),
                                    ctypes.POINTER(i32), ctypes.POINTER(i32)]
         L.orc_schedule.restype = i64
         L.orc_free.argtypes = [vp]
         L.orc_free.restype = None
-        L.orc_replay.argtypes = [i32, i32, i32, i32, i64, i32, i32, i64, vp, vp, i64, vp]
+        L.orc_replay.argtypes = [i32, i32, i32, i32, i32, i64, i32, i32, i64, vp, vp, i64, vp]
         L.orc_replay.restype = i32
-        L.orc_replay_sym.argtypes = [i32, i32, i32, i32, i64, i32, i64, vp, i64, vp]
+        L.orc_replay_sym.argtypes = [i32, i32, i32, i32, i32, i64, i32, i64, vp, i64, vp]
         L.orc_replay_sym.restype = i32
         L.orc_sym_reset.argtypes = []
         L.orc_sym_reset.restype = None
@@ -113,11 +113,12 @@ def slicer(algo, coll, P, n, dtype, loop_bytes, p_intra=1):
     return c.value, nl.value, t.value
 
 
-def schedule(algo, coll, P, n, dtype="float32", loop_bytes=0, p_intra=1):
-    """Message list (numpy structured array, MSG_DTYPE), steps per loop, loops."""
+def schedule(algo, coll, P, n, dtype="float32", loop_bytes=0, p_intra=1, root=0):
+    """Message list (numpy structured array, MSG_DTYPE), steps per loop, loops.
+    root is used by the broadcast only."""
     ptr = ctypes.POINTER(_Msg)()
     spl, nl = ctypes.c_int32(), ctypes.c_int32()
-    m = lib().orc_schedule(ALGOS[algo], COLLS[coll], P, p_intra, n, DTYPES[dtype], loop_bytes,
+    m = lib().orc_schedule(ALGOS[algo], COLLS[coll], P, p_intra, root, n, DTYPES[dtype], loop_bytes,
                            ctypes.byref(ptr), ctypes.byref(spl), ctypes.byref(nl))
     if m < 0:
         raise ValueError("bad schedule arguments")
@@ -139,13 +140,13 @@ def _check_X(X, dtype):
     return X
 
 
-def replay(algo, coll, X, op, dtype, loop_bytes=0, p_intra=1, J=None):
+def replay(algo, coll, X, op, dtype, loop_bytes=0, p_intra=1, J=None, root=0):
     """Step-by-step replay of the schedule on rank vectors X (P, n).
 
     Returns (P, len(J)) values after the schedule (J = all elements by default):
     for allreduce every row is that rank's output; for reducescatter rank r's
     result is its row restricted to segment r; for allgather every row is the
-    gathered vector.
+    gathered vector; for broadcast every row is the root's vector.
     """
     X = _check_X(X, dtype)
     P, n = X.shape
@@ -155,14 +156,14 @@ def replay(algo, coll, X, op, dtype, loop_bytes=0, p_intra=1, J=None):
         J = np.ascontiguousarray(J, dtype=np.int64)
         Jp, nJ = J.ctypes.data, J.size
     Y = np.empty((P, nJ), dtype=NP_DTYPE[dtype])
-    rc = lib().orc_replay(ALGOS[algo], COLLS[coll], P, p_intra, n, DTYPES[dtype], OPS[op],
+    rc = lib().orc_replay(ALGOS[algo], COLLS[coll], P, p_intra, root, n, DTYPES[dtype], OPS[op],
                           loop_bytes, X.ctypes.data, Jp, nJ, Y.ctypes.data)
     if rc:
         raise ValueError("oracle replay rejected its arguments")
     return Y
 
 
-def replay_sym(algo, coll, P, n, layout_dtype="float32", loop_bytes=0, p_intra=1, J=None):
+def replay_sym(algo, coll, P, n, layout_dtype="float32", loop_bytes=0, p_intra=1, J=None, root=0):
     """Symbolic replay: (P, len(J)) int64 expression node ids."""
     if J is None:
         Jp, nJ = None, n
@@ -170,7 +171,7 @@ def replay_sym(algo, coll, P, n, layout_dtype="float32", loop_bytes=0, p_intra=1
         J = np.ascontiguousarray(J, dtype=np.int64)
         Jp, nJ = J.ctypes.data, J.size
     Y = np.empty((P, nJ), dtype=np.int64)
-    rc = lib().orc_replay_sym(ALGOS[algo], COLLS[coll], P, p_intra, n, DTYPES[layout_dtype],
+    rc = lib().orc_replay_sym(ALGOS[algo], COLLS[coll], P, p_intra, root, n, DTYPES[layout_dtype],
                               loop_bytes, Jp, nJ, Y.ctypes.data)
     if rc:
         raise ValueError("oracle symbolic replay rejected its arguments")

@@ -23,6 +23,8 @@
  *  - Pipeline: "AllGather 算子的 Pipeline 时序编排", "Rank0 视角" and Table 1
  *    of the HCCL Pipeline article: inter-server ring overlapped with an
  *    intra-server full mesh, p_inter steps per phase.
+ *  - Broadcast: Table 1 of the HCCL RHD article, Broadcast row (root parity
+ *    picks the part1 members, distance halving, one last send).
  *
  * Model of execution.  A schedule is a list of messages.  A message
  * (step, kind, src, dst, seg) sends the PRE-STEP value of segment seg held by
@@ -64,7 +66,7 @@
 #define ORC_MAX_P 256
 
 enum { ORC_RING = 0, ORC_RHD = 1, ORC_PIPE = 2 };
-enum { ORC_AR = 0, ORC_RS = 1, ORC_AG = 2 };
+enum { ORC_AR = 0, ORC_RS = 1, ORC_AG = 2, ORC_BCAST = 3 };
 enum { ORC_I32 = 0, ORC_F32 = 1, ORC_BF16 = 2, ORC_SYM = 3 };
 enum { ORC_SUM = 0, ORC_PROD = 1, ORC_MAX = 2, ORC_MIN = 3 };
 enum { ORC_REDUCE = 0, ORC_COPY = 1 };
@@ -118,6 +120,7 @@ static int log2_exact(int q) { int t = 0; while ((1 << t) < q) t++; return t; }
  */
 int orc_num_segments(int algo, int coll, int P) {
     if (P < 1) return 0;
+    if (coll == ORC_BCAST) return 1;  /* the whole vector moves as one block */
     if (algo == ORC_RHD && coll == ORC_AR) return pow2_floor(P);
     return P;
 }
@@ -394,6 +397,46 @@ static int gen_rhd(proto_vec* pv, int coll, int P) {
 }
 
 /*
+ * RHD Broadcast (Table 1 of the RHD article, Broadcast row): the root's
+ * parity decides whether the even or the odd rank of each part1 pair
+ * (2i, 2i+1), i < r, joins the power-of-two block; inside the block the data
+ * spreads by distance halving (partner = v XOR p'/2, then p'/4, ..., 1, every
+ * holder sending to its partner); one last step sends from each part1 block
+ * member to its pair partner.  ceil(log2 P) steps, each moving n elements.
+ */
+static int gen_rhd_bcast(proto_vec* pv, int P, int root) {
+    int pp = pow2_floor(P);
+    int r = P - pp;
+    int par = root & 1;
+    int vroot = root < 2 * r ? root / 2 : root - r;
+    char* have = (char*)calloc((size_t)pp, 1);
+    char* next = (char*)calloc((size_t)pp, 1);
+    if (!have || !next) { free(have); free(next); return -1; }
+    have[vroot] = 1;
+    for (int d = pp / 2; d >= 1; d /= 2) {
+        memcpy(next, have, (size_t)pp);
+        for (int v = 0; v < pp; v++) {
+            if (!have[v]) continue;
+            int u = v ^ d;
+            int rv = v < r ? 2 * v + par : v + r;
+            int ru = u < r ? 2 * u + par : u + r;
+            if (pv_push(pv, ORC_COPY, rv, ru, 0)) { free(have); free(next); return -1; }
+            next[u] = 1;
+        }
+        memcpy(have, next, (size_t)pp);
+        pv_end_step(pv);
+    }
+    free(have);
+    free(next);
+    if (r > 0) {
+        for (int i = 0; i < r; i++)
+            if (pv_push(pv, ORC_COPY, 2 * i + par, 2 * i + 1 - par, 0)) return -1;
+        pv_end_step(pv);
+    }
+    return 0;
+}
+
+/*
  * Hierarchical Pipeline, P = p_inter x p_intra, rank = s * p_intra + l
  * (server-major), inter ring s -> s+1 among ranks of equal local index l.
  * AllGather (the narrated case): at step t = 1..p_inter every rank (s,l)
@@ -445,7 +488,8 @@ static int gen_pipe(proto_vec* pv, int coll, int P, int p_intra) {
 
 static int check_args(int algo, int coll, int P, int p_intra, int64_t n, int dtype) {
     if (algo < ORC_RING || algo > ORC_PIPE) return -1;
-    if (coll < ORC_AR || coll > ORC_AG) return -1;
+    if (coll < ORC_AR || coll > ORC_BCAST) return -1;
+    if (coll == ORC_BCAST && algo != ORC_RHD) return -1;  /* only the RHD broadcast is described */
     if (P < 1 || P > ORC_MAX_P) return -1;
     if (n < 0) return -1;
     if (elem_size(dtype) == 0) return -1;
@@ -459,13 +503,16 @@ static int check_args(int algo, int coll, int P, int p_intra, int64_t n, int dty
  * whose slice is empty are dropped).  Returns the number of messages, or -1.
  * The caller frees *out with orc_free.
  */
-static int64_t build_schedule(int algo, int coll, int P, int p_intra, int64_t n, int dtype,
-                              int64_t loop_bytes, orc_msg** out, int* steps_per_loop, int* nloops) {
+static int64_t build_schedule(int algo, int coll, int P, int p_intra, int root, int64_t n,
+                              int dtype, int64_t loop_bytes, orc_msg** out, int* steps_per_loop,
+                              int* nloops) {
     *out = NULL;
     if (check_args(algo, coll, P, p_intra, n, dtype)) return -1;
+    if (root < 0 || root >= P) return -1;
     proto_vec pv = {0};
     int rc;
-    if (algo == ORC_RING) rc = gen_ring(&pv, coll, P);
+    if (coll == ORC_BCAST) rc = gen_rhd_bcast(&pv, P, root);
+    else if (algo == ORC_RING) rc = gen_ring(&pv, coll, P);
     else if (algo == ORC_RHD) rc = gen_rhd(&pv, coll, P);
     else rc = gen_pipe(&pv, coll, P, p_intra);
     if (rc) { free(pv.v); return -1; }
@@ -504,10 +551,12 @@ static int64_t build_schedule(int algo, int coll, int P, int p_intra, int64_t n,
     return m;
 }
 
-/* Exported: the schedule as a message list (test suite reads it). */
-int64_t orc_schedule(int algo, int coll, int P, int p_intra, int64_t n, int dtype,
+/* Exported: the schedule as a message list (test suite reads it).  root is
+ * used by the Broadcast only. */
+int64_t orc_schedule(int algo, int coll, int P, int p_intra, int root, int64_t n, int dtype,
                      int64_t loop_bytes, orc_msg** out, int* steps_per_loop, int* nloops) {
-    return build_schedule(algo, coll, P, p_intra, n, dtype, loop_bytes, out, steps_per_loop, nloops);
+    return build_schedule(algo, coll, P, p_intra, root, n, dtype, loop_bytes, out, steps_per_loop,
+                          nloops);
 }
 
 void orc_free(void* p) { free(p); }
@@ -626,9 +675,9 @@ static int64_t lower_bound(const int64_t* J, int64_t nJ, int64_t x) {
  * schedule fails to deliver is visible.
  * Returns 0, or -1 on bad arguments / allocation failure.
  */
-static int replay_impl(int algo, int coll, int P, int p_intra, int64_t n, int dtype, int ldtype,
-                       int op, int64_t loop_bytes, const void* X, const int64_t* J, int64_t nJ,
-                       void* Y) {
+static int replay_impl(int algo, int coll, int P, int p_intra, int root, int64_t n, int dtype,
+                       int ldtype, int op, int64_t loop_bytes, const void* X, const int64_t* J,
+                       int64_t nJ, void* Y) {
     if (check_args(algo, coll, P, p_intra, n, ldtype)) return -1;
     if (ldtype == ORC_SYM) return -1;
     if (op < ORC_SUM || op > ORC_MIN) return -1;
@@ -647,7 +696,8 @@ static int replay_impl(int algo, int coll, int P, int p_intra, int64_t n, int dt
 
     orc_msg* msgs = NULL;
     int spl = 0, loops = 0;
-    int64_t nm = build_schedule(algo, coll, P, p_intra, n, ldtype, loop_bytes, &msgs, &spl, &loops);
+    int64_t nm = build_schedule(algo, coll, P, p_intra, root, n, ldtype, loop_bytes, &msgs, &spl,
+                                &loops);
     if (nm < 0) { free(Jall); return -1; }
 
     size_t cells = (size_t)P * (size_t)(nJ > 0 ? nJ : 1);
@@ -666,6 +716,7 @@ static int replay_impl(int algo, int coll, int P, int p_intra, int64_t n, int dt
                     seg_range(L, n, q, &slo, &shi);
                     if (J[i] < slo || J[i] >= shi) v = SYM_POISON;
                 }
+                if (coll == ORC_BCAST && q != root) v = SYM_POISON;
             } else {
                 v = load_raw(dtype, X, (int64_t)q * n + J[i]);
             }
@@ -701,18 +752,18 @@ static int replay_impl(int algo, int coll, int P, int p_intra, int64_t n, int dt
     return 0;
 }
 
-int orc_replay(int algo, int coll, int P, int p_intra, int64_t n, int dtype, int op,
+int orc_replay(int algo, int coll, int P, int p_intra, int root, int64_t n, int dtype, int op,
                int64_t loop_bytes, const void* X, const int64_t* J, int64_t nJ, void* Y) {
     if (dtype == ORC_SYM) return -1;
-    return replay_impl(algo, coll, P, p_intra, n, dtype, dtype, op, loop_bytes, X, J, nJ, Y);
+    return replay_impl(algo, coll, P, p_intra, root, n, dtype, dtype, op, loop_bytes, X, J, nJ, Y);
 }
 
 /* Symbolic replay: the schedule of a layout dtype (its 16-byte segment
  * rounding), every value an expression node; Y holds P x nJ int64 node ids
  * (read them back with orc_sym_string / orc_sym_leaves). */
-int orc_replay_sym(int algo, int coll, int P, int p_intra, int64_t n, int layout_dtype,
+int orc_replay_sym(int algo, int coll, int P, int p_intra, int root, int64_t n, int layout_dtype,
                    int64_t loop_bytes, const int64_t* J, int64_t nJ, int64_t* Y) {
-    return replay_impl(algo, coll, P, p_intra, n, ORC_SYM, layout_dtype, ORC_SUM, loop_bytes,
+    return replay_impl(algo, coll, P, p_intra, root, n, ORC_SYM, layout_dtype, ORC_SUM, loop_bytes,
                        NULL, J, nJ, Y);
 }
 

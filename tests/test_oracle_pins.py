@@ -813,3 +813,50 @@ def test_bad_arguments_rejected():
         O.replay("ring", "allreduce", X, "sum", "float32", J=np.array([3, 2]))
     with pytest.raises(ValueError):
         O.schedule("ring", "allreduce", 0, 10)
+
+
+# ---------------------------------------------------------------------------
+# RHD Broadcast (Table 1 of the RHD article, Broadcast row)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("P", list(range(1, 41)) + [63, 64])
+def test_broadcast_every_rank_gets_the_root_exactly(P):
+    n = 20
+    for root in range(P):
+        O.sym_reset()
+        Y = O.replay_sym("rhd", "broadcast", P, n, root=root)
+        for r in range(P):
+            cnt = O.sym_leaves(Y[r, 0])
+            want = np.zeros_like(cnt)
+            want[root] = 1
+            assert np.array_equal(cnt, want), (P, root, r)
+        X = hc_inputs.uniform_int32(P, n, seed=P * 100 + root)
+        Yn = O.replay("rhd", "broadcast", X, "sum", "int32", root=root)
+        assert np.all(Yn == X[root][None, :])
+
+
+@pytest.mark.parametrize("P", list(range(1, 65)))
+def test_broadcast_schedule_table1(P):
+    """ceil(log2 P) steps of n elements each (the row's ceil(log p)(a + n b));
+    every non-root rank receives exactly once, the root never; the part1 ranks
+    of the root's parity join the distance-halving block and each then sends
+    once to its pair partner."""
+    n = 64
+    pp = 1 << (P.bit_length() - 1)
+    r = P - pp
+    for root in range(P):
+        msgs, spl, _ = O.schedule("rhd", "broadcast", P, n, root=root)
+        assert spl == (math.ceil(math.log2(P)) if P > 1 else 0)
+        assert np.all(msgs["hi"] - msgs["lo"] == n) and np.all(msgs["kind"] == O.COPY)
+        recv = np.bincount(msgs["dst"], minlength=P)
+        assert recv[root] == 0 and all(recv[q] == 1 for q in range(P) if q != root)
+        par = root & 1
+        for s in steps_of(msgs):
+            srcs, dsts = s["src"].tolist(), s["dst"].tolist()
+            assert len(set(srcs)) == len(srcs) and len(set(dsts)) == len(dsts)
+        core = msgs[msgs["step"] < spl - (1 if r else 0)]
+        for q in set(core["src"].tolist()) | set(core["dst"].tolist()):
+            assert q >= 2 * r or q % 2 == par
+        if r:
+            last = msgs[msgs["step"] == spl - 1]
+            assert sorted(zip(last["src"].tolist(), last["dst"].tolist())) == \
+                [(2 * i + par, 2 * i + 1 - par) for i in range(r)]
