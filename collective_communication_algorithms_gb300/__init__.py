@@ -8,12 +8,14 @@ the C entry points; allreduce / reduce_scatter / allgather accept lists of
 torch CUDA tensors (one per virtual rank) and pass their pointers and the
 current CUDA stream.  PyTorch only provides device memory and streams.
 """
-from ._binding import (ALGOS, COLLS, DTYPES, MODES, OPS, HcError, hc_allgather, hc_allreduce,
+from ._binding import (ALGOS, COLLS, DTYPES, MODES, OPS, Graph, HcError, hc_allgather, hc_allreduce,
+                       hc_broadcast,
                        hc_num_segments, hc_reduce_scatter, hc_schedule_stats, hc_scratch_bytes,
                        hc_segment_range, hc_step_plan, hc_version, lib, make_opts)
 from ._binding import LIB_PATH as library_path
 
-__all__ = ["allreduce", "reduce_scatter", "allgather", "segment_range", "segments",
+__all__ = ["allreduce", "reduce_scatter", "allgather", "broadcast", "segment_range", "segments",
+           "Graph", "hc_broadcast",
            "hc_allreduce", "hc_reduce_scatter", "hc_allgather", "hc_segment_range",
            "hc_num_segments", "hc_scratch_bytes", "hc_schedule_stats", "hc_step_plan",
            "hc_version", "HcError", "make_opts", "library_path", "lib"]
@@ -85,4 +87,13 @@ def allgather(send, recv, algo="ring", mode="fused", ranks_per_server=1, max_loo
     hc_allgather(None if send is None else _ptrs(send), _ptrs(recv), P, recv[0].numel(),
                  _dtype_name(recv[0]), algo, _opts(mode, ranks_per_server, max_loop_bytes, None),
                  _stream(stream))
+    return recv
+
+
+def broadcast(send, recv, root=0, algo="rhd", mode="fused", stream=None):
+    """recv[r] = send (the root's vector) for every rank; send=None: in place
+    from recv[root]."""
+    P = len(recv)
+    hc_broadcast(None if send is None else send.data_ptr(), _ptrs(recv), P, recv[0].numel(),
+                 _dtype_name(recv[0]), root, algo, _opts(mode, 1, 0, None), _stream(stream))
     return recv

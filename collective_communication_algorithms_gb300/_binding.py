@@ -16,7 +16,7 @@ MAX_RANKS = 64
 DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
 ALGOS = {"ring": 0, "rhd": 1, "pipeline": 2}
-COLLS = {"allreduce": 0, "reducescatter": 1, "allgather": 2}
+COLLS = {"allreduce": 0, "reducescatter": 1, "allgather": 2, "broadcast": 3}
 MODES = {"fused": 0, "step": 1}
 STATUS = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_UNSUPPORTED", 3: "HC_ERR_ALIGN",
           4: "HC_ERR_SCRATCH", 5: "HC_ERR_CUDA", 6: "HC_ERR_TIMEOUT"}
@@ -60,8 +60,9 @@ class hc_plan_record_t(ctypes.Structure):
 
 # every symbol include/hc.h declares
 EXPORTS = ("hc_allreduce", "hc_reduce_scatter", "hc_reduce_scatter_static_scratch",
-           "hc_allgather", "hc_segment_range", "hc_graph_create", "hc_graph_add_allreduce",
-           "hc_graph_add_reduce_scatter", "hc_graph_add_allgather", "hc_graph_build",
+           "hc_allgather", "hc_broadcast", "hc_segment_range", "hc_graph_create",
+           "hc_graph_add_allreduce", "hc_graph_add_reduce_scatter", "hc_graph_add_allgather",
+           "hc_graph_add_broadcast", "hc_graph_build",
            "hc_graph_launch", "hc_graph_info", "hc_graph_destroy",
            "hc_num_segments", "hc_scratch_bytes", "hc_schedule_stats", "hc_step_plan",
            "hc_device_status", "hc_last_cuda_error", "hc_status_string", "hc_version")
@@ -97,6 +98,11 @@ def lib():
         L.hc_graph_add_allgather.argtypes = [vp, ptrs, ptrs, i32, sz, i32, i32,
                                              ctypes.POINTER(hc_opts_t)]
         L.hc_graph_add_allgather.restype = i32
+        L.hc_graph_add_broadcast.argtypes = [vp, vp, ptrs, i32, sz, i32, i32, i32,
+                                             ctypes.POINTER(hc_opts_t)]
+        L.hc_graph_add_broadcast.restype = i32
+        L.hc_broadcast.argtypes = [vp, ptrs, i32, sz, i32, i32, i32, ctypes.POINTER(hc_opts_t), vp]
+        L.hc_broadcast.restype = i32
         for name in ("hc_graph_build", "hc_graph_destroy"):
             getattr(L, name).argtypes = [vp]
             getattr(L, name).restype = i32
@@ -116,7 +122,7 @@ def lib():
                                         ctypes.POINTER(hc_stats_t),
                                         ctypes.POINTER(ctypes.c_ulonglong)]
         L.hc_schedule_stats.restype = i32
-        L.hc_step_plan.argtypes = [i32, i32, i32, i32, sz, i32, sz, i32,
+        L.hc_step_plan.argtypes = [i32, i32, i32, i32, sz, i32, sz, i32, i32,
                                    ctypes.POINTER(hc_plan_record_t), sz,
                                    ctypes.POINTER(sz), ctypes.POINTER(i32)]
         L.hc_step_plan.restype = i32
@@ -203,6 +209,15 @@ def hc_allgather(send, recv, P, count, dtype, algo, opts=None, stream=0):
     _check(st, "hc_allgather")
 
 
+def hc_broadcast(send, recv, P, count, dtype, root, algo="rhd", opts=None, stream=0):
+    """send: device pointer of the root's vector, or 0/None for in place."""
+    st = lib().hc_broadcast(ctypes.c_void_p(int(send)) if send else None, _ptr_array(recv), int(P),
+                            int(count), _enum(DTYPES, dtype), int(root), _enum(ALGOS, algo),
+                            ctypes.byref(opts) if opts is not None else None,
+                            ctypes.c_void_p(int(stream)) if stream else None)
+    _check(st, "hc_broadcast")
+
+
 def hc_segment_range(algo, coll, P, count, dtype, k):
     off, ln = ctypes.c_size_t(), ctypes.c_size_t()
     _check(lib().hc_segment_range(_enum(ALGOS, algo), _enum(COLLS, coll), int(P), int(count),
@@ -233,13 +248,13 @@ def hc_schedule_stats(algo, coll, P, count, dtype, ranks_per_server=1, max_loop_
 
 
 def hc_step_plan(algo, coll, P, count, dtype, ranks_per_server=1, max_loop_bytes=0,
-                 in_place=True):
+                 in_place=True, root=0):
     """Returns (list of record dicts, number of launches)."""
     L = lib()
     n = ctypes.c_size_t()
     nl = ctypes.c_int()
     args = (_enum(ALGOS, algo), _enum(COLLS, coll), int(P), int(ranks_per_server), int(count),
-            _enum(DTYPES, dtype), int(max_loop_bytes), 1 if in_place else 0)
+            _enum(DTYPES, dtype), int(max_loop_bytes), 1 if in_place else 0, int(root))
     _check(L.hc_step_plan(*args, None, 0, ctypes.byref(n), ctypes.byref(nl)), "hc_step_plan")
     recs = (hc_plan_record_t * max(1, n.value))()
     _check(L.hc_step_plan(*args, recs, n.value, ctypes.byref(n), ctypes.byref(nl)),
@@ -288,6 +303,13 @@ class Graph:
                                             _enum(ALGOS, algo),
                                             ctypes.byref(opts) if opts is not None else None),
                "hc_graph_add_allgather")
+
+    def add_broadcast(self, send, recv, P, count, dtype, root, algo="rhd", opts=None):
+        _check(lib().hc_graph_add_broadcast(self.handle, ctypes.c_void_p(int(send)) if send else None,
+                                            _ptr_array(recv), int(P), int(count),
+                                            _enum(DTYPES, dtype), int(root), _enum(ALGOS, algo),
+                                            ctypes.byref(opts) if opts is not None else None),
+               "hc_graph_add_broadcast")
 
     def build(self):
         _check(lib().hc_graph_build(self.handle), "hc_graph_build")

@@ -19,7 +19,8 @@ bool valid_dtype(hc_dtype_t d) { return d == HC_INT32 || d == HC_FLOAT32 || d ==
 bool valid_op(hc_op_t o) { return o == HC_SUM || o == HC_PROD || o == HC_MAX || o == HC_MIN; }
 bool valid_algo(hc_algo_t a) { return a == HC_ALGO_RING || a == HC_ALGO_RHD || a == HC_ALGO_PIPELINE; }
 bool valid_coll(hc_coll_t c) {
-    return c == HC_COLL_ALLREDUCE || c == HC_COLL_REDUCE_SCATTER || c == HC_COLL_ALLGATHER;
+    return c == HC_COLL_ALLREDUCE || c == HC_COLL_REDUCE_SCATTER || c == HC_COLL_ALLGATHER ||
+           c == HC_COLL_BROADCAST;
 }
 
 struct Opts {
@@ -81,27 +82,28 @@ int sm_count_of_current_device() {
 }
 
 // ---------------------------------------------------------------- plan cache
-using PlanKey = std::tuple<int, int, int, int, int64_t, int, int64_t, unsigned long long,
+using PlanKey = std::tuple<int, int, int, int, int, int64_t, int, int64_t, unsigned long long,
                            unsigned long long>;
 std::map<PlanKey, std::shared_ptr<const Plan>>& plan_cache() {
     static std::map<PlanKey, std::shared_ptr<const Plan>> m;
     return m;
 }
 
-std::shared_ptr<const Plan> get_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n,
-                     hc_dtype_t dt, int64_t loop_bytes, const Aliasing& al) {
+std::shared_ptr<const Plan> get_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root,
+                                     int64_t n, hc_dtype_t dt, int64_t loop_bytes,
+                                     const Aliasing& al) {
     unsigned long long m1 = 0, m2 = 0;
     for (int r = 0; r < P; r++) {
         if (al.orig_is_work[r]) m1 |= 1ull << r;
         if (al.final_is_work[r]) m2 |= 1ull << r;
     }
-    PlanKey key{(int)algo, (int)coll, P, p_intra, n, (int)dt, loop_bytes, m1, m2};
+    PlanKey key{(int)algo, (int)coll, P, p_intra, root, n, (int)dt, loop_bytes, m1, m2};
     auto& cache = plan_cache();
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;
     if (cache.size() >= 256) cache.clear();  // plans still held by callers stay alive
     auto plan = std::make_shared<Plan>();
-    if (!build_plan(algo, coll, P, p_intra, n, dt, loop_bytes, al, plan.get())) return nullptr;
+    if (!build_plan(algo, coll, P, p_intra, root, n, dt, loop_bytes, al, plan.get())) return nullptr;
     cache.emplace(key, plan);
     return plan;
 }
@@ -117,11 +119,14 @@ namespace hc {
 
 // Validate one collective call and record everything its launch needs.
 hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, int P, size_t count,
-                    hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts,
+                    hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts, int root,
                     Prepared* out) {
     *out = Prepared();
     if (!valid_dtype(dtype) || !valid_op(op) || !valid_algo(algo)) return HC_ERR_INVALID_ARG;
     if (P < 1 || P > kMaxRanks) return HC_ERR_INVALID_ARG;
+    const bool bcast = coll == HC_COLL_BROADCAST;
+    if (bcast && (root < 0 || root >= P)) return HC_ERR_INVALID_ARG;
+    if (bcast && algo != HC_ALGO_RHD) return HC_ERR_UNSUPPORTED;
     Opts o;
     hc_status_t st = read_opts(opts, algo, P, &o);
     if (st != HC_OK) return st;
@@ -134,12 +139,13 @@ hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, 
     c.count = count;
     c.mode = o.mode;
     c.p_intra = o.p_intra;
+    c.root = bcast ? root : -1;
     c.loop_bytes = o.loop_bytes;
     c.empty = count == 0;
     if (c.empty) return HC_OK;
     if (count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
     if (!recv) return HC_ERR_INVALID_ARG;
-    if (!send && coll != HC_COLL_ALLGATHER) return HC_ERR_INVALID_ARG;
+    if (!send && coll != HC_COLL_ALLGATHER && !bcast) return HC_ERR_INVALID_ARG;
 
     const int64_t n = (int64_t)count;
     const int es = elem_bytes(dtype);
@@ -150,9 +156,10 @@ hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, 
     // of an empty trailing segment) is never touched: it may be NULL or
     // unaligned; every other buffer must be non-null and 16-byte aligned
     for (int r = 0; r < P; r++) {
-        const bool seg_empty = own.seg_hi(r) == own.seg_lo(r);
+        const bool seg_empty = bcast ? false : own.seg_hi(r) == own.seg_lo(r);
         const bool recv_used = !(coll == HC_COLL_REDUCE_SCATTER && seg_empty);
-        const bool send_used = send && !(coll == HC_COLL_ALLGATHER && seg_empty);
+        const bool send_used = bcast ? (send && r == root && send[r])
+                                     : send && !(coll == HC_COLL_ALLGATHER && seg_empty);
         if ((recv_used && !recv[r]) || (send_used && !send[r])) return HC_ERR_INVALID_ARG;
         if ((recv_used && ((uintptr_t)recv[r] & 15)) || (send_used && ((uintptr_t)send[r] & 15)))
             return HC_ERR_ALIGN;
@@ -188,6 +195,24 @@ hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, 
                 c.writes.push_back({d, d + len});
             } else {
                 c.writes.push_back({s, s + full});  // the input is working memory
+            }
+        } else if (bcast) {
+            // only the root has an input; it is in place when it is recv[root]
+            const uintptr_t s = (r == root && send && send[r]) ? (uintptr_t)send[r] : d;
+            c.send[r] = s;
+            c.ag_in_place[r] = (s == d);
+            c.al.orig_is_work[r] = c.ag_in_place[r];
+            c.al.final_is_work[r] = true;
+            if (r == root && s != d) {
+                iv.push_back({s, s + full});
+                c.reads.push_back({s, s + full});
+            }
+            if (r != root || s != d) {
+                iv.push_back({d, d + full});
+                c.writes.push_back({d, d + full});
+            } else {
+                iv.push_back({d, d + full});
+                c.reads.push_back({d, d + full});
             }
         } else {
             const uintptr_t off = (uintptr_t)own.seg_lo(r) * es;
@@ -226,7 +251,7 @@ hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, 
     }
     if (any_overlap(iv)) return HC_ERR_INVALID_ARG;
     if (o.mode == HC_MODE_STEP) {
-        c.plan = get_plan(algo, coll, P, o.p_intra, n, dtype, o.loop_bytes, c.al);
+        c.plan = get_plan(algo, coll, P, o.p_intra, bcast ? root : 0, n, dtype, o.loop_bytes, c.al);
         if (!c.plan) return HC_ERR_INVALID_ARG;
     }
     return HC_OK;
@@ -259,6 +284,7 @@ hc_status_t execute(const Prepared& c, cudaStream_t stream) {
         a.recv = rp;
         std::memcpy(a.ag_in_place, c.ag_in_place, sizeof a.ag_in_place);
         std::memcpy(a.rs_in_place, c.rs_in_place, sizeof a.rs_in_place);
+        a.root = c.root;
         return cuda_status(launch_fused(a, stream, sms));
     }
     uintptr_t base[LOC_COUNT][kMaxRanks];
@@ -273,6 +299,10 @@ hc_status_t execute(const Prepared& c, cudaStream_t stream) {
             base[LOC_ORIG][r] = s;
             base[LOC_WORK][r] = c.rs_in_place[r] ? s : c.scratch + (uintptr_t)r * scratch_stride(c.count, c.dtype);
             base[LOC_FINAL][r] = d - (uintptr_t)own.seg_lo(r) * es;
+        } else if (c.coll == HC_COLL_BROADCAST) {
+            base[LOC_ORIG][r] = s;
+            base[LOC_WORK][r] = d;
+            base[LOC_FINAL][r] = d;
         } else {
             const uintptr_t off = (uintptr_t)own.seg_lo(r) * es;
             base[LOC_ORIG][r] = s - off;
@@ -301,7 +331,7 @@ hc_status_t run(hc_coll_t coll, const void* const* send, void* const* recv, int 
                 hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts,
                 cudaStream_t stream) {
     Prepared c;
-    const hc_status_t st = prepare(coll, send, recv, P, count, dtype, op, algo, opts, &c);
+    const hc_status_t st = prepare(coll, send, recv, P, count, dtype, op, algo, opts, -1, &c);
     if (st != HC_OK) return st;
     return execute(c, stream);
 }
@@ -322,6 +352,19 @@ hc_status_t hc_reduce_scatter(const void* const* send, void* const* recv, int P,
                               const hc_opts_t* opts, hc_stream_t stream) {
     return run(HC_COLL_REDUCE_SCATTER, send, recv, P, count, dtype, op, algo, opts,
                (cudaStream_t)stream);
+}
+
+hc_status_t hc_broadcast(const void* send, void* const* recv, int P, size_t count,
+                         hc_dtype_t dtype, int root, hc_algo_t algo, const hc_opts_t* opts,
+                         hc_stream_t stream) {
+    if (P < 1 || P > kMaxRanks) return HC_ERR_INVALID_ARG;
+    const void* sendv[kMaxRanks] = {nullptr};
+    if (root >= 0 && root < P) sendv[root] = send;
+    Prepared c;
+    const hc_status_t st = prepare(HC_COLL_BROADCAST, sendv, recv, P, count, dtype, HC_SUM, algo,
+                                   opts, root, &c);
+    if (st != HC_OK) return st;
+    return execute(c, (cudaStream_t)stream);
 }
 
 hc_status_t hc_allgather(const void* const* send, void* const* recv, int P, size_t count,
@@ -363,14 +406,14 @@ hc_status_t hc_schedule_stats(hc_algo_t algo, hc_coll_t coll, int P, int ranks_p
     if (p_intra < 1 || P % p_intra) return HC_ERR_INVALID_ARG;
     const int64_t n = (int64_t)count;
     int spl = 0;
-    if (!schedule_traffic(algo, coll, P, p_intra, n, dtype, (int64_t)max_loop_bytes, &spl,
+    if (!schedule_traffic(algo, coll, P, p_intra, 0, n, dtype, (int64_t)max_loop_bytes, &spl,
                           bytes_sent))
         return HC_ERR_INVALID_ARG;
     if (!stats) return HC_OK;
     Aliasing al;
     for (int r = 0; r < P; r++) { al.orig_is_work[r] = true; al.final_is_work[r] = true; }
     Plan plan;
-    if (!build_plan(algo, coll, P, p_intra, n, dtype, (int64_t)max_loop_bytes, al, &plan))
+    if (!build_plan(algo, coll, P, p_intra, 0, n, dtype, (int64_t)max_loop_bytes, al, &plan))
         return HC_ERR_INVALID_ARG;
     const int es = elem_bytes(dtype);
     stats->steps_per_loop = spl;
@@ -392,14 +435,14 @@ hc_status_t hc_schedule_stats(hc_algo_t algo, hc_coll_t coll, int P, int ranks_p
     stats->step_bytes = sb;
     const unsigned long long nb = (unsigned long long)n * es;
     if (coll == HC_COLL_ALLREDUCE) stats->fused_bytes = 2ull * P * nb;
-    else if (coll == HC_COLL_REDUCE_SCATTER) stats->fused_bytes = (unsigned long long)(P + 1) * nb;
-    else stats->fused_bytes = (unsigned long long)(P + 1) * nb;
+    else stats->fused_bytes = (unsigned long long)(P + 1) * nb;  // RS, AG and Broadcast out of place
     return HC_OK;
 }
 
 hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_server,
                          size_t count, hc_dtype_t dtype, size_t max_loop_bytes, int in_place,
-                         hc_plan_record_t* records, size_t cap, size_t* n_out, int* launches) {
+                         int root, hc_plan_record_t* records, size_t cap, size_t* n_out,
+                         int* launches) {
     if (!valid_algo(algo) || !valid_coll(coll) || !valid_dtype(dtype) || !n_out)
         return HC_ERR_INVALID_ARG;
     if (P < 1 || P > kMaxRanks || count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
@@ -410,11 +453,12 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
         al.orig_is_work[r] = in_place != 0;
         al.final_is_work[r] = in_place != 0;
         if (coll == HC_COLL_ALLREDUCE) al.final_is_work[r] = true;
-        if (coll == HC_COLL_ALLGATHER) al.final_is_work[r] = true;
+        if (coll == HC_COLL_ALLGATHER || coll == HC_COLL_BROADCAST) al.final_is_work[r] = true;
     }
+    if (coll == HC_COLL_BROADCAST && (root < 0 || root >= P)) return HC_ERR_INVALID_ARG;
     Plan plan;
-    if (!build_plan(algo, coll, P, p_intra, (int64_t)count, dtype, (int64_t)max_loop_bytes, al,
-                    &plan))
+    if (!build_plan(algo, coll, P, p_intra, coll == HC_COLL_BROADCAST ? root : 0, (int64_t)count,
+                    dtype, (int64_t)max_loop_bytes, al, &plan))
         return HC_ERR_INVALID_ARG;
     size_t m = 0;
     for (size_t li = 0; li < plan.launches.size(); li++) {

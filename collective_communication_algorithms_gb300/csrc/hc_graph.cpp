@@ -41,10 +41,11 @@ void release(hc_graph_s* g) {
 }
 
 hc_status_t add(hc_graph_t g, hc_coll_t coll, const void* const* send, void* const* recv, int P,
-                size_t count, hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts) {
+                size_t count, hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts,
+                int root = -1) {
     if (!g) return HC_ERR_INVALID_ARG;
     Prepared c;
-    const hc_status_t st = prepare(coll, send, recv, P, count, dtype, op, algo, opts, &c);
+    const hc_status_t st = prepare(coll, send, recv, P, count, dtype, op, algo, opts, root, &c);
     if (st != HC_OK) return st;
     std::vector<int> d;
     for (int i = 0; i < (int)g->nodes.size(); i++)
@@ -81,6 +82,15 @@ hc_status_t hc_graph_add_allgather(hc_graph_t g, const void* const* send, void* 
                                    size_t count, hc_dtype_t dtype, hc_algo_t algo,
                                    const hc_opts_t* opts) {
     return add(g, HC_COLL_ALLGATHER, send, recv, P, count, dtype, HC_SUM, algo, opts);
+}
+
+hc_status_t hc_graph_add_broadcast(hc_graph_t g, const void* send, void* const* recv, int P,
+                                   size_t count, hc_dtype_t dtype, int root, hc_algo_t algo,
+                                   const hc_opts_t* opts) {
+    if (P < 1 || P > kMaxRanks) return HC_ERR_INVALID_ARG;
+    const void* sendv[kMaxRanks] = {nullptr};
+    if (root >= 0 && root < P) sendv[root] = send;
+    return add(g, HC_COLL_BROADCAST, sendv, recv, P, count, dtype, HC_SUM, algo, opts, root);
 }
 
 hc_status_t hc_graph_build(hc_graph_t g) {

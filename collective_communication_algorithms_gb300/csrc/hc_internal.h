@@ -107,11 +107,11 @@ struct Aliasing {
 };
 
 // Build the step-mode plan (host only).  Returns false on bad arguments.
-bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n, hc_dtype_t dt,
-                int64_t loop_bytes, const Aliasing& alias, Plan* out);
+bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root, int64_t n,
+                hc_dtype_t dt, int64_t loop_bytes, const Aliasing& alias, Plan* out);
 
 // Per-rank bytes sent over the whole schedule and steps per loop (host only).
-bool schedule_traffic(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n,
+bool schedule_traffic(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root, int64_t n,
                       hc_dtype_t dt, int64_t loop_bytes, int* steps_per_loop,
                       unsigned long long* bytes_sent);
 
@@ -134,6 +134,7 @@ struct FusedArgs {
     void* const* recv;
     bool ag_in_place[kMaxRanks];
     bool rs_in_place[kMaxRanks];
+    int root;  // Broadcast root, -1 otherwise
 };
 
 // ---------------------------------------------------------------------------
@@ -152,6 +153,7 @@ struct Prepared {
     hc_mode_t mode = HC_MODE_FUSED;
     int P = 0;
     int p_intra = 1;
+    int root = -1;  // Broadcast root
     int64_t loop_bytes = 0;
     size_t count = 0;
     bool empty = true;
@@ -167,8 +169,9 @@ struct Prepared {
     std::vector<Interval> reads, writes;
 };
 
+// root: Broadcast root (-1 for the other collectives)
 hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, int P, size_t count,
-                    hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts,
+                    hc_dtype_t dtype, hc_op_t op, hc_algo_t algo, const hc_opts_t* opts, int root,
                     Prepared* out);
 hc_status_t execute(const Prepared& c, cudaStream_t stream);
 // true when b must wait for a (a write of one overlaps a read or write of the other)

@@ -203,7 +203,8 @@ struct FusedParams {
     int pp;                    // RHD: power-of-two core size
     int rfold;                 // RHD: number of folded pairs
     int stages;                // TMA kernels: pipeline depth
-    unsigned long long skip_mask;  // AllGather: ranks whose own segment is already in place
+    int owner;                 // Broadcast: the root owns the single segment (-1: segment k's owner is k)
+    unsigned long long skip_mask;  // AllGather / Broadcast: ranks whose data is already in place
 };
 
 constexpr int kFusedThreads = 256;
@@ -372,12 +373,14 @@ fused_reduce(const __grid_constant__ FusedParams p) {
 
 // AllGather, register path: segment k read once from its owner, written to
 // every rank (the owner's own copy only when it is not already in place).
+// Broadcast is the same kernel with one segment owned by the root.
 template <int ES>
 __global__ void __launch_bounds__(kFusedThreads)
 fused_allgather(const __grid_constant__ FusedParams p) {
     constexpr int A = 16 / ES;
-    const int k = blockIdx.y;
-    const int64_t sbeg = (int64_t)k * p.L;
+    const int seg = blockIdx.y;
+    const int k = p.owner >= 0 ? p.owner : seg;
+    const int64_t sbeg = (int64_t)seg * p.L;
     if (sbeg >= p.n) return;
     const int64_t send_ = (sbeg + p.L < p.n) ? sbeg + p.L : p.n;
     const int64_t nfull = (send_ - sbeg) / A;
@@ -473,13 +476,15 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 // AllGather, TMA-staged: one thread streams the owner's segment through
 // shared memory in 8 KB tiles, each tile loaded once and bulk-stored to every
 // rank (the owner's own copy only when it is not already in place).
+// Broadcast: one segment owned by the root.
 template <int ES>
 __global__ void __launch_bounds__(32)
 fused_allgather_tma(const __grid_constant__ FusedParams p) {
     constexpr int A = 16 / ES;
     extern __shared__ __align__(128) unsigned char smem[];
-    const int k = blockIdx.y;
-    const int64_t sbeg = (int64_t)k * p.L;
+    const int seg = blockIdx.y;
+    const int k = p.owner >= 0 ? p.owner : seg;
+    const int64_t sbeg = (int64_t)seg * p.L;
     const int64_t send_ = sbeg + p.L < p.n ? sbeg + p.L : p.n;
     const int64_t nfull = send_ > sbeg ? (send_ - sbeg) / A : 0;
     const bool skip_own = (p.skip_mask >> k) & 1ull;
@@ -664,8 +669,15 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     std::memset(&p, 0, sizeof p);
     const int es = elem_bytes(a.dtype);
     const Layout& lay = a.lay;
+    p.owner = -1;
     for (int r = 0; r < a.P; r++) {
-        if (a.coll == HC_COLL_ALLGATHER) {
+        if (a.coll == HC_COLL_BROADCAST) {
+            // the root's input is the whole vector (segment 0 starts at 0)
+            p.src[r] = (uintptr_t)(a.send && a.send[r] ? a.send[r] : a.recv[r]);
+            p.dst[r] = (uintptr_t)a.recv[r];
+            if (a.ag_in_place[r]) p.skip_mask |= 1ull << r;
+            p.owner = a.root;
+        } else if (a.coll == HC_COLL_ALLGATHER) {
             // owner's segment view: send[k] holds segment k from its start
             const uintptr_t seg_off = (uintptr_t)lay.seg_lo(r) * es;
             const uintptr_t s = a.send ? (uintptr_t)a.send[r] : (uintptr_t)a.recv[r] + seg_off;
@@ -692,7 +704,7 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     const int64_t seg_bytes = lay.L * es;
     void* args[] = {&p};
 
-    if (a.coll == HC_COLL_ALLGATHER) {
+    if (a.coll == HC_COLL_ALLGATHER || a.coll == HC_COLL_BROADCAST) {
         // TMA path once every segment holds several tiles per block
         if (seg_bytes >= 16 * (int64_t)kAgTile) {
             void* fn = es == 2 ? (void*)fused_allgather_tma<2> : (void*)fused_allgather_tma<4>;

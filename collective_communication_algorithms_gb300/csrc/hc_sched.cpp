@@ -288,8 +288,53 @@ void pipe_steps(hc_coll_t coll, int P, int pin, std::vector<LStep>& st) {
     }
 }
 
-bool logical_steps(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, std::vector<LStep>& st) {
+// ---------------------------------------------------------------- Broadcast
+// RHD Broadcast: part1 members of the root's parity join the power-of-two
+// block, distance halving spreads the vector (partner v ^ p'/2, ..., v ^ 1),
+// then each part1 member sends it to its pair partner.
+void rhd_bcast_steps(int P, int root, std::vector<LStep>& st) {
+    const int pp = core_size(P);
+    const int r = P - pp;
+    const int par = root & 1;
+    auto real = [r, par](int v) { return v < r ? 2 * v + par : v + r; };
+    std::vector<char> have(pp, 0);
+    have[root < 2 * r ? root / 2 : root - r] = 1;
+    for (int d = pp / 2; d >= 1; d >>= 1) {
+        LStep x;
+        std::vector<char> nxt = have;
+        for (int v = 0; v < pp; v++) {
+            if (!have[v]) continue;
+            LItem it;
+            it.outs = one(real(v ^ d));
+            it.ins = one(real(v));
+            it.segs = {0};
+            x.push_back(it);
+            nxt[v ^ d] = 1;
+        }
+        have = nxt;
+        st.push_back(x);
+    }
+    if (r) {
+        LStep x;
+        for (int i = 0; i < r; i++) {
+            LItem it;
+            it.outs = one(2 * i + 1 - par);
+            it.ins = one(2 * i + par);
+            it.segs = {0};
+            x.push_back(it);
+        }
+        st.push_back(x);
+    }
+}
+
+bool logical_steps(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root,
+                   std::vector<LStep>& st) {
     st.clear();
+    if (coll == HC_COLL_BROADCAST) {
+        if (algo != HC_ALGO_RHD || root < 0 || root >= P) return false;
+        rhd_bcast_steps(P, root, st);
+        return true;
+    }
     if (algo == HC_ALGO_RING) ring_steps(coll, P, st);
     else if (algo == HC_ALGO_RHD) rhd_steps(coll, P, st);
     else if (algo == HC_ALGO_PIPELINE) {
@@ -355,6 +400,7 @@ DevItem make_item(const RankSet& outs, uint8_t out_loc, int acc, uint8_t acc_loc
 // ---------------------------------------------------------------------------
 int num_segments(hc_algo_t algo, hc_coll_t coll, int P) {
     if (P < 1) return 0;
+    if (coll == HC_COLL_BROADCAST) return 1;
     if (algo == HC_ALGO_RHD && coll == HC_COLL_ALLREDUCE) return core_size(P);
     return P;
 }
@@ -391,11 +437,11 @@ Slicing make_slicing(hc_algo_t algo, int P, int p_intra, const Layout& lay, hc_d
     return s;
 }
 
-bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n, hc_dtype_t dt,
-                int64_t loop_bytes, const Aliasing& alias, Plan* out) {
+bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root, int64_t n,
+                hc_dtype_t dt, int64_t loop_bytes, const Aliasing& alias, Plan* out) {
     if (P < 1 || P > kMaxRanks || n < 0) return false;
     std::vector<LStep> steps;
-    if (!logical_steps(algo, coll, P, p_intra, steps)) return false;
+    if (!logical_steps(algo, coll, P, p_intra, root, steps)) return false;
     Plan& plan = *out;
     plan = Plan();
     plan.lay = make_layout(algo, coll, P, n, dt);
@@ -408,6 +454,10 @@ bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n, h
     if (coll == HC_COLL_ALLGATHER) {
         std::fill(state.begin(), state.end(), LOC_NONE);
         for (int q = 0; q < P; q++) state[(size_t)q * S + q] = LOC_ORIG;
+    }
+    if (coll == HC_COLL_BROADCAST) {
+        std::fill(state.begin(), state.end(), LOC_NONE);
+        state[(size_t)root * S] = LOC_ORIG;
     }
     auto st_at = [&](int q, int k) -> uint8_t& { return state[(size_t)q * S + k]; };
 
@@ -423,6 +473,9 @@ bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n, h
                     items.push_back(make_item(one(q), LOC_WORK, -1, 0, one(q), LOC_ORIG,
                                               SegPattern{q, 1, 1, 1}));
         }
+        if (si == 0 && coll == HC_COLL_BROADCAST && !alias.orig_is_work[root])
+            items.push_back(make_item(one(root), LOC_WORK, -1, 0, one(root), LOC_ORIG,
+                                      SegPattern{0, 1, 1, 1}));
         for (const LItem& li : steps[si]) {
             // group segments by the locations of their operands
             std::map<std::pair<int, int>, std::vector<int>> groups;
@@ -444,6 +497,7 @@ bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n, h
                 for (int k : li.segs) st_at(li.outs.at(o), k) = LOC_WORK;
         if (si == 0 && coll == HC_COLL_ALLGATHER)
             for (int q = 0; q < P; q++) st_at(q, q) = LOC_WORK;
+        if (si == 0 && coll == HC_COLL_BROADCAST) st_at(root, 0) = LOC_WORK;
         bound.push_back(items);
     }
 
@@ -493,11 +547,11 @@ bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n, h
     return true;
 }
 
-bool schedule_traffic(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n,
+bool schedule_traffic(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root, int64_t n,
                       hc_dtype_t dt, int64_t loop_bytes, int* steps_per_loop,
                       unsigned long long* bytes_sent) {
     std::vector<LStep> steps;
-    if (P < 1 || P > kMaxRanks || !logical_steps(algo, coll, P, p_intra, steps)) return false;
+    if (P < 1 || P > kMaxRanks || !logical_steps(algo, coll, P, p_intra, root, steps)) return false;
     (void)loop_bytes;
     Layout lay = make_layout(algo, coll, P, n, dt);
     const int b = elem_bytes(dt);

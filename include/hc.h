@@ -92,7 +92,12 @@ typedef enum {
 typedef enum { HC_INT32 = 0, HC_FLOAT32 = 1, HC_BFLOAT16 = 2 } hc_dtype_t;
 typedef enum { HC_SUM = 0, HC_PROD = 1, HC_MAX = 2, HC_MIN = 3 } hc_op_t;
 typedef enum { HC_ALGO_RING = 0, HC_ALGO_RHD = 1, HC_ALGO_PIPELINE = 2 } hc_algo_t;
-typedef enum { HC_COLL_ALLREDUCE = 0, HC_COLL_REDUCE_SCATTER = 1, HC_COLL_ALLGATHER = 2 } hc_coll_t;
+typedef enum {
+    HC_COLL_ALLREDUCE = 0,
+    HC_COLL_REDUCE_SCATTER = 1,
+    HC_COLL_ALLGATHER = 2,
+    HC_COLL_BROADCAST = 3
+} hc_coll_t;
 
 /*
  * HC_MODE_FUSED: one kernel reads every rank's element once, reduces it in
@@ -157,6 +162,25 @@ hc_status_t hc_allreduce(const void* const* send, void* const* recv, int P, size
 hc_status_t hc_reduce_scatter(const void* const* send, void* const* recv, int P, size_t count,
                               hc_dtype_t dtype, hc_op_t op, hc_algo_t algo,
                               const hc_opts_t* opts, hc_stream_t stream);
+
+/*
+ * Broadcast: recv[r][j] = root's vector[j] for every rank r and j < count
+ * (RHD article, Table 1, Broadcast row: the root's parity decides whether the
+ * even or the odd rank of each non-power-of-two part1 pair joins the
+ * power-of-two block; the block spreads the data by distance halving and
+ * each part1 member then sends it once to its pair partner; ceil(log2 P)
+ * steps).  The segment layout is one segment, the whole vector.
+ *  send    : device pointer to the root's count elements, or NULL when the
+ *            data already sits in recv[root] (in place; also when send ==
+ *            recv[root]).
+ *  recv[r] : count elements of rank r's output.
+ *  root    : 0 <= root < P.
+ *  algo    : HC_ALGO_RHD (the pages describe no other broadcast);
+ *            anything else returns HC_ERR_UNSUPPORTED.
+ */
+hc_status_t hc_broadcast(const void* send, void* const* recv, int P, size_t count,
+                         hc_dtype_t dtype, int root, hc_algo_t algo, const hc_opts_t* opts,
+                         hc_stream_t stream);
 
 /*
  * ReduceScatter for callers that may not allocate device memory.  The pages
@@ -235,6 +259,9 @@ hc_status_t hc_graph_add_reduce_scatter(hc_graph_t graph, const void* const* sen
 hc_status_t hc_graph_add_allgather(hc_graph_t graph, const void* const* send, void* const* recv,
                                    int P, size_t count, hc_dtype_t dtype, hc_algo_t algo,
                                    const hc_opts_t* opts);
+hc_status_t hc_graph_add_broadcast(hc_graph_t graph, const void* send, void* const* recv, int P,
+                                   size_t count, hc_dtype_t dtype, int root, hc_algo_t algo,
+                                   const hc_opts_t* opts);
 hc_status_t hc_graph_build(hc_graph_t graph);
 hc_status_t hc_graph_launch(hc_graph_t graph, hc_stream_t stream);
 hc_status_t hc_graph_info(hc_graph_t graph, int* collectives, int* edges, int* kernels);
@@ -250,7 +277,8 @@ int hc_num_segments(hc_algo_t algo, hc_coll_t coll, int P);
 size_t hc_scratch_bytes(hc_algo_t algo, int P, size_t count, hc_dtype_t dtype);
 
 /*
- * Schedule statistics (host only, no GPU needed).
+ * Schedule statistics (host only, no GPU needed; a Broadcast is counted
+ * with root 0, every root giving the same counts).
  *  steps_per_loop : communication steps of one loop (Ring AllReduce 2(P-1),
  *                   RHD 2 ceil(log2 P), Pipeline 2 p_inter, ...)
  *  loops, chunk, tail : the loop slicer's result (elements per segment)
@@ -286,6 +314,7 @@ hc_status_t hc_schedule_stats(hc_algo_t algo, hc_coll_t coll, int P, int ranks_p
  * ReduceScatter output (recv).  Every record computes, for lo <= j < hi,
  *   out[o][j] = (acc (+)) in[0][j] (+) in[1][j] (+) ... for each o in outs.
  * `in_place` says which buffers alias (nonzero: every rank in place).
+ * `root` is the Broadcast root (ignored by the other collectives).
  */
 typedef struct {
     int32_t launch;
@@ -303,7 +332,8 @@ typedef struct {
 
 hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_server,
                          size_t count, hc_dtype_t dtype, size_t max_loop_bytes, int in_place,
-                         hc_plan_record_t* records, size_t cap, size_t* n, int* launches);
+                         int root, hc_plan_record_t* records, size_t cap, size_t* n,
+                         int* launches);
 
 /*
  * Device-side status of the kernels that wait on shared-memory barriers (the

@@ -57,11 +57,13 @@ def segments(algo, coll, P, n, dtype):
 
 
 def run_collective(coll, algo, X, dtype, op="sum", mode="fused", in_place=False, p_intra=1,
-                   loop_bytes=0, stream=0):
+                   loop_bytes=0, stream=0, root=0):
     """Run one collective through the C ABI on rank vectors X (P, n).
     Returns (results, guards_ok): results[r] is rank r's output (AR/AG: n
     elements; RS: its segment)."""
     P, n = X.shape
+    if coll == "broadcast":
+        return _run_broadcast(algo, X, dtype, mode, in_place, root, stream)
     segs = segments(algo, coll, P, n, dtype)
     regions = []
     send_ptrs, recv_ptrs = [], []
@@ -141,3 +143,22 @@ def expected(coll, Y, segs):
 
 def same_bits(a, b, dtype):
     return np.array_equal(_as_int(a, dtype), _as_int(b, dtype))
+
+
+def _run_broadcast(algo, X, dtype, mode, in_place, root, stream):
+    P, n = X.shape
+    regions = [Region(dtype, n) for _ in range(P)]
+    send = 0
+    if in_place:
+        regions[root].write(X[root])
+    else:
+        src = Region(dtype, n)
+        src.write(X[root])
+        regions.append(src)
+        send = src.ptr
+    opts = B.make_opts(mode)
+    torch.cuda.synchronize()
+    B.hc_broadcast(send, [regions[r].ptr for r in range(P)], P, n, dtype, root, algo, opts, stream)
+    torch.cuda.synchronize()
+    res = [regions[r].read(0, n) for r in range(P)]
+    return res, all(r.guards_ok() for r in regions)

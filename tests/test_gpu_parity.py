@@ -194,6 +194,24 @@ def test_tma_staged_paths(algo, dtype):
     assert B.hc_device_status() == 0
 
 
+@pytest.mark.parametrize("mode", ["fused", "step"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_broadcast(mode, dtype):
+    """RHD Broadcast: every rank ends with the root's vector, bit for bit."""
+    for P in (1, 2, 3, 5, 8, 12, 16):
+        roots = range(P) if P <= 8 else (0, 1, P // 2, P - 1)
+        for n in (1, 37, 4099, 80000 + 3):
+            X = inputs(dtype, P, n, seed=P * 13 + n, op="sum")
+            for root in roots:
+                for in_place in (False, True):
+                    res, ok = run_collective("broadcast", "rhd", X, dtype, mode=mode,
+                                             in_place=in_place, root=root)
+                    assert ok, "a write landed outside its buffer"
+                    Y = O.replay("rhd", "broadcast", X, "sum", dtype, root=root)
+                    for r in range(P):
+                        assert same_bits(res[r], Y[r], dtype), (P, n, root, r, in_place)
+
+
 def test_zz_no_device_timeouts_recorded():
     """No bounded device-side wait gave up during the GPU tests above."""
     from collective_communication_algorithms_gb300 import _binding as B

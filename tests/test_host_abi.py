@@ -144,7 +144,7 @@ def check_races(recs, coll, in_place):
                 raise AssertionError("write/write race")
 
 
-def check_bounds(recs, algo, coll, P, n, dtype):
+def check_bounds(recs, algo, coll, P, n, dtype, root=None):
     """Every record stays inside its segment (hence inside the rank vector),
     names valid ranks, and reads a rank's input (location 0) of an
     AllGather only inside that rank's own segment."""
@@ -157,6 +157,8 @@ def check_bounds(recs, algo, coll, P, n, dtype):
         assert 1 <= len(r["in_ranks"]) and 1 <= len(r["out_ranks"])
         if coll == "allgather" and r["in_loc"] == 0:
             assert r["in_ranks"] == [r["seg"]]
+        if coll == "broadcast" and r["in_loc"] == 0 and root is not None:
+            assert r["in_ranks"] == [root]
         if coll == "reducescatter" and r["out_loc"] == 2:
             assert r["out_ranks"] == [r["seg"]]
 
@@ -430,3 +432,40 @@ def test_graph_dependency_analysis():
     with pytest.raises(B.HcError):
         g.launch()  # not built
     g.close()
+
+
+def test_broadcast_steps_traffic_and_plans():
+    """RHD Broadcast: steps and per-rank traffic equal the oracle's; the step
+    plans (every root, in place and out of place) are race-free, in bounds
+    and, executed on the CPU, leave the root's vector on every rank."""
+    for P in (1, 2, 3, 4, 5, 6, 7, 8, 12, 16, 33, 64):
+        n = 16 * P + 3
+        st, sent = B.hc_schedule_stats("rhd", "broadcast", P, n, "float32")
+        msgs, spl, _ = O.schedule("rhd", "broadcast", P, n, "float32", root=0)
+        assert st["steps_per_loop"] == spl
+        want = np.zeros(P, dtype=np.int64)
+        np.add.at(want, msgs["src"], (msgs["hi"] - msgs["lo"]) * 4)
+        assert list(want) == sent
+    for P in (1, 2, 3, 5, 8, 12):
+        n = 1000 + P
+        for root in range(P):
+            X = hc_inputs.uniform_int32(P, n, seed=P * 10 + root)
+            for in_place in (True, False):
+                recs, _ = B.hc_step_plan("rhd", "broadcast", P, n, "int32", 1, 0, in_place, root)
+                check_races(recs, "allgather", in_place)
+                check_bounds(recs, "rhd", "broadcast", P, n, "int32", root)
+                bufs = Buffers("broadcast", X, in_place, [(0, n)] * P, fill=-7)
+                if not in_place:
+                    # only the root's input exists; its output starts unset
+                    for r in range(P):
+                        if r != root:
+                            bufs.orig[r][:] = -9
+                execute(recs, bufs, lambda a, b: (a + b).astype(np.int32))
+                for r in range(P):
+                    assert np.array_equal(bufs.work[r], X[root]), (P, root, r, in_place)
+
+
+def test_broadcast_rejects_other_algorithms():
+    with pytest.raises(B.HcError) as e:
+        B.hc_step_plan("ring", "broadcast", 4, 100, "float32")
+    assert e.value.status == 1
