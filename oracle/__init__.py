@@ -17,7 +17,7 @@ import numpy as np
 
 from . import build as _build
 
-ALGOS = {"ring": 0, "rhd": 1, "pipeline": 2}
+ALGOS = {"ring": 0, "rhd": 1, "pipeline": 2, "hier": 3}
 COLLS = {"allreduce": 0, "reducescatter": 1, "allgather": 2, "broadcast": 3}
 DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
@@ -49,11 +49,11 @@ def lib():
         path = _build.build()
         L = ctypes.CDLL(path)
         i32, i64, vp = ctypes.c_int, ctypes.c_int64, ctypes.c_void_p
-        L.orc_num_segments.argtypes = [i32, i32, i32]
+        L.orc_num_segments.argtypes = [i32, i32, i32, i32]
         L.orc_num_segments.restype = i32
-        L.orc_seg_stride.argtypes = [i32, i32, i32, i64, i32]
+        L.orc_seg_stride.argtypes = [i32, i32, i32, i32, i64, i32]
         L.orc_seg_stride.restype = i64
-        L.orc_segment.argtypes = [i32, i32, i32, i64, i32, i32,
+        L.orc_segment.argtypes = [i32, i32, i32, i32, i64, i32, i32,
                                   ctypes.POINTER(i64), ctypes.POINTER(i64)]
         L.orc_segment.restype = i32
         L.orc_slicer.argtypes = [i32, i32, i32, i32, i64, i32, i64,
@@ -87,22 +87,23 @@ def library_path() -> str:
     return _build.LIB
 
 
-def num_segments(algo, coll, P):
-    return lib().orc_num_segments(ALGOS[algo], COLLS[coll], P)
+def num_segments(algo, coll, P, p_intra=1):
+    return lib().orc_num_segments(ALGOS[algo], COLLS[coll], P, p_intra)
 
 
-def segment(algo, coll, P, n, dtype, k):
+def segment(algo, coll, P, n, dtype, k, p_intra=1):
     """(offset, length) of segment k."""
     off, ln = ctypes.c_int64(), ctypes.c_int64()
-    rc = lib().orc_segment(ALGOS[algo], COLLS[coll], P, n, DTYPES[dtype], k,
+    rc = lib().orc_segment(ALGOS[algo], COLLS[coll], P, p_intra, n, DTYPES[dtype], k,
                            ctypes.byref(off), ctypes.byref(ln))
     if rc:
         raise ValueError("bad segment index")
     return off.value, ln.value
 
 
-def segments(algo, coll, P, n, dtype):
-    return [segment(algo, coll, P, n, dtype, k) for k in range(num_segments(algo, coll, P))]
+def segments(algo, coll, P, n, dtype, p_intra=1):
+    return [segment(algo, coll, P, n, dtype, k, p_intra)
+            for k in range(num_segments(algo, coll, P, p_intra))]
 
 
 def slicer(algo, coll, P, n, dtype, loop_bytes, p_intra=1):

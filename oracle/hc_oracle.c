@@ -25,6 +25,12 @@
  *    intra-server full mesh, p_inter steps per phase.
  *  - Broadcast: Table 1 of the HCCL RHD article, Broadcast row (root parity
  *    picks the part1 members, distance halving, one last send).
+ *  - Plain hierarchical AllReduce: intra-server ReduceScatter, inter-server
+ *    RHD AllReduce, intra-server AllGather (Pipeline article, "与其它分级算法
+ *    的关系"; RHD article, "耗时模型解读").  Its floating-point association
+ *    order (the RHD tree over servers of intra-server chains rotated from the
+ *    local index) is a reading; parity unpinned beyond the definition,
+ *    exactly-once contributions and the step / traffic counts.
  *
  * Model of execution.  A schedule is a list of messages.  A message
  * (step, kind, src, dst, seg) sends the PRE-STEP value of segment seg held by
@@ -65,7 +71,7 @@
 
 #define ORC_MAX_P 256
 
-enum { ORC_RING = 0, ORC_RHD = 1, ORC_PIPE = 2 };
+enum { ORC_RING = 0, ORC_RHD = 1, ORC_PIPE = 2, ORC_HIER = 3 };
 enum { ORC_AR = 0, ORC_RS = 1, ORC_AG = 2, ORC_BCAST = 3 };
 enum { ORC_I32 = 0, ORC_F32 = 1, ORC_BF16 = 2, ORC_SYM = 3 };
 enum { ORC_SUM = 0, ORC_PROD = 1, ORC_MAX = 2, ORC_MIN = 3 };
@@ -118,15 +124,21 @@ static int log2_exact(int q) { int t = 0; while ((1 << t) < q) t++; return t; }
  * 16 bytes; segment k = [min(kL, n), min((k+1)L, n)).  Trailing segments may
  * be short or empty.
  */
-int orc_num_segments(int algo, int coll, int P) {
+int orc_num_segments(int algo, int coll, int P, int p_intra) {
     if (P < 1) return 0;
     if (coll == ORC_BCAST) return 1;  /* the whole vector moves as one block */
     if (algo == ORC_RHD && coll == ORC_AR) return pow2_floor(P);
+    if (algo == ORC_HIER) {
+        /* p_intra intra-server segments, each cut into the p' blocks of the
+         * inter-server RHD over the P / p_intra servers */
+        if (p_intra < 1 || P % p_intra) return 0;
+        return p_intra * pow2_floor(P / p_intra);
+    }
     return P;
 }
 
-int64_t orc_seg_stride(int algo, int coll, int P, int64_t n, int dtype) {
-    int S = orc_num_segments(algo, coll, P);
+int64_t orc_seg_stride(int algo, int coll, int P, int p_intra, int64_t n, int dtype) {
+    int S = orc_num_segments(algo, coll, P, p_intra);
     int64_t A = 16 / elem_size(dtype);
     if (S <= 0 || n <= 0) return 0;
     return ceil_div64(ceil_div64(n, S), A) * A;
@@ -137,11 +149,11 @@ static void seg_range(int64_t L, int64_t n, int k, int64_t* lo, int64_t* hi) {
     *hi = min64((int64_t)(k + 1) * L, n);
 }
 
-int orc_segment(int algo, int coll, int P, int64_t n, int dtype, int k,
+int orc_segment(int algo, int coll, int P, int p_intra, int64_t n, int dtype, int k,
                 int64_t* off, int64_t* len) {
-    int S = orc_num_segments(algo, coll, P);
+    int S = orc_num_segments(algo, coll, P, p_intra);
     if (k < 0 || k >= S) return -1;
-    int64_t L = orc_seg_stride(algo, coll, P, n, dtype);
+    int64_t L = orc_seg_stride(algo, coll, P, p_intra, n, dtype);
     int64_t lo, hi;
     seg_range(L, n, k, &lo, &hi);
     *off = lo;
@@ -158,15 +170,15 @@ int orc_segment(int algo, int coll, int P, int64_t n, int dtype, int k,
  * its own.  The pages give no formula.  Reading used: with a byte limit Sb per
  * loop, every rank holds `slots` segment slices of c elements for each of the
  * P peers:   c = align_down(Sb / (P * slots * b), 128 / b),
- * slots = 1 (Ring), ceil(P/2) (RHD), p_intra - 1 (Pipeline, at least 1).
+ * slots = 1 (Ring), ceil(P/2) (RHD), p_intra - 1 (Pipeline and the plain
+ * hierarchical AllReduce, at least 1).
  * The 128-byte alignment is the DMA granule of the AllReduce section.
  * Sb == 0 means a single loop.  Loop i covers [i*c, min((i+1)*c, len_k)) of
  * every segment k; the last loop is the tail.
  */
 int orc_slicer(int algo, int coll, int P, int p_intra, int64_t n, int dtype,
                int64_t loop_bytes, int64_t* chunk, int* loops, int64_t* tail) {
-    (void)coll;
-    int64_t L = orc_seg_stride(algo, coll, P, n, dtype);
+    int64_t L = orc_seg_stride(algo, coll, P, p_intra, n, dtype);
     int b = elem_size(dtype);
     if (L <= 0 || loop_bytes <= 0) {
         *chunk = L; *loops = 1; *tail = L;
@@ -174,7 +186,7 @@ int orc_slicer(int algo, int coll, int P, int p_intra, int64_t n, int dtype,
     }
     int64_t slots = 1;
     if (algo == ORC_RHD) slots = (P + 1) / 2;
-    if (algo == ORC_PIPE) slots = (p_intra - 1 > 1) ? (p_intra - 1) : 1;
+    if (algo == ORC_PIPE || algo == ORC_HIER) slots = (p_intra - 1 > 1) ? (p_intra - 1) : 1;
     int64_t granule = 128 / b;
     int64_t c = loop_bytes / ((int64_t)P * slots * b);
     c = (c / granule) * granule;
@@ -486,8 +498,105 @@ static int gen_pipe(proto_vec* pv, int coll, int P, int p_intra) {
     return 0;
 }
 
+/*
+ * Plain hierarchical AllReduce (the Pipeline article's "与其它分级算法的关系":
+ * Server 内 ReduceScatter -> Server 间 AllReduce -> Server 内 AllGather; the
+ * RHD article's "耗时模型解读" puts RHD at the inter-server level and
+ * Mesh / Ring inside the server).  Reading used: P = p_inter x p_intra,
+ * rank = s * p_intra + l; the intra-server phases are full-mesh steps; the
+ * inter-server AllReduce is the RHD AllReduce (fold, halving, doubling,
+ * unfold) among the ranks of equal local index l, on intra segment l.
+ * Segments: intra segment l is made of the p' blocks l*p' .. l*p' + p' - 1
+ * (p' = 2^floor(log2 p_inter)).
+ *  step A (if p_intra > 1): (s,l) receives every block of intra segment l
+ *    from (s,l+1), (s,l+2), ... and folds them into its own;
+ *  steps B: RHD AllReduce over servers within each local index;
+ *  step C (if p_intra > 1): (s,l) copies intra segment l to every (s,l').
+ */
+static int gen_hier(proto_vec* pv, int P, int pin) {
+    const int pout = P / pin;
+    const int pp = pow2_floor(pout);
+    const int r = pout - pp;
+    const int lg = log2_exact(pp);
+    #define HR(s, l) ((s) * pin + (l))
+    #define SV(v) ((v) < r ? 2 * (v) : (v) + r)
+    if (pin > 1) {
+        for (int s = 0; s < pout; s++)
+            for (int l = 0; l < pin; l++)
+                for (int j = 1; j < pin; j++)
+                    for (int b = 0; b < pp; b++)
+                        if (pv_push(pv, ORC_REDUCE, HR(s, mod_int(l + j, pin)), HR(s, l), l * pp + b))
+                            return -1;
+        pv_end_step(pv);
+    }
+    if (r > 0) {
+        for (int l = 0; l < pin; l++)
+            for (int i = 0; i < r; i++)
+                for (int b = 0; b < pp; b++)
+                    if (pv_push(pv, ORC_REDUCE, HR(2 * i + 1, l), HR(2 * i, l), l * pp + b)) return -1;
+        pv_end_step(pv);
+    }
+    int* wlo = (int*)malloc(sizeof(int) * pp);
+    int* whi = (int*)malloc(sizeof(int) * pp);
+    int* nlo = (int*)malloc(sizeof(int) * pp);
+    int* nhi = (int*)malloc(sizeof(int) * pp);
+    if (!wlo || !whi || !nlo || !nhi) { free(wlo); free(whi); free(nlo); free(nhi); return -1; }
+    int rc = 0;
+    for (int v = 0; v < pp; v++) { wlo[v] = 0; whi[v] = pp; }
+    for (int t = 0; t < lg && !rc; t++) {
+        for (int v = 0; v < pp; v++) {
+            int u = v ^ (1 << t), mid = (wlo[v] + whi[v]) / 2;
+            int keep_low = ((v >> t) & 1) == 0;
+            int glo = keep_low ? mid : wlo[v], ghi = keep_low ? whi[v] : mid;
+            for (int l = 0; l < pin && !rc; l++)
+                for (int k = glo; k < ghi && !rc; k++)
+                    rc = pv_push(pv, ORC_REDUCE, HR(SV(v), l), HR(SV(u), l), l * pp + k);
+            nlo[v] = keep_low ? wlo[v] : mid;
+            nhi[v] = keep_low ? mid : whi[v];
+        }
+        memcpy(wlo, nlo, sizeof(int) * pp);
+        memcpy(whi, nhi, sizeof(int) * pp);
+        pv_end_step(pv);
+    }
+    for (int t = lg - 1; t >= 0 && !rc; t--) {
+        for (int v = 0; v < pp; v++) {
+            int u = v ^ (1 << t);
+            for (int l = 0; l < pin && !rc; l++)
+                for (int k = wlo[v]; k < whi[v] && !rc; k++)
+                    rc = pv_push(pv, ORC_COPY, HR(SV(v), l), HR(SV(u), l), l * pp + k);
+            nlo[v] = wlo[v] < wlo[u] ? wlo[v] : wlo[u];
+            nhi[v] = whi[v] > whi[u] ? whi[v] : whi[u];
+        }
+        memcpy(wlo, nlo, sizeof(int) * pp);
+        memcpy(whi, nhi, sizeof(int) * pp);
+        pv_end_step(pv);
+    }
+    free(wlo); free(whi); free(nlo); free(nhi);
+    if (rc) return -1;
+    if (r > 0) {
+        for (int l = 0; l < pin; l++)
+            for (int i = 0; i < r; i++)
+                for (int b = 0; b < pp; b++)
+                    if (pv_push(pv, ORC_COPY, HR(2 * i, l), HR(2 * i + 1, l), l * pp + b)) return -1;
+        pv_end_step(pv);
+    }
+    if (pin > 1) {
+        for (int s = 0; s < pout; s++)
+            for (int l = 0; l < pin; l++)
+                for (int j = 1; j < pin; j++)
+                    for (int b = 0; b < pp; b++)
+                        if (pv_push(pv, ORC_COPY, HR(s, l), HR(s, mod_int(l + j, pin)), l * pp + b))
+                            return -1;
+        pv_end_step(pv);
+    }
+    #undef HR
+    #undef SV
+    return 0;
+}
+
 static int check_args(int algo, int coll, int P, int p_intra, int64_t n, int dtype) {
-    if (algo < ORC_RING || algo > ORC_PIPE) return -1;
+    if (algo < ORC_RING || algo > ORC_HIER) return -1;
+    if (algo == ORC_HIER && (coll != ORC_AR || p_intra < 1 || P % p_intra)) return -1;
     if (coll < ORC_AR || coll > ORC_BCAST) return -1;
     if (coll == ORC_BCAST && algo != ORC_RHD) return -1;  /* only the RHD broadcast is described */
     if (P < 1 || P > ORC_MAX_P) return -1;
@@ -512,6 +621,7 @@ static int64_t build_schedule(int algo, int coll, int P, int p_intra, int root, 
     proto_vec pv = {0};
     int rc;
     if (coll == ORC_BCAST) rc = gen_rhd_bcast(&pv, P, root);
+    else if (algo == ORC_HIER) rc = gen_hier(&pv, P, p_intra);
     else if (algo == ORC_RING) rc = gen_ring(&pv, coll, P);
     else if (algo == ORC_RHD) rc = gen_rhd(&pv, coll, P);
     else rc = gen_pipe(&pv, coll, P, p_intra);
@@ -519,7 +629,7 @@ static int64_t build_schedule(int algo, int coll, int P, int p_intra, int root, 
     int64_t c, tail;
     int loops;
     orc_slicer(algo, coll, P, p_intra, n, dtype, loop_bytes, &c, &loops, &tail);
-    int64_t L = orc_seg_stride(algo, coll, P, n, dtype);
+    int64_t L = orc_seg_stride(algo, coll, P, p_intra, n, dtype);
     int64_t cap = pv.n * (int64_t)loops;
     orc_msg* v = (orc_msg*)malloc(sizeof(orc_msg) * (size_t)(cap > 0 ? cap : 1));
     if (!v) { free(pv.v); return -1; }
@@ -705,7 +815,7 @@ static int replay_impl(int algo, int coll, int P, int p_intra, int root, int64_t
     uint64_t* nxt = (uint64_t*)malloc(sizeof(uint64_t) * cells);
     if (!cur || !nxt) { free(cur); free(nxt); free(msgs); free(Jall); return -1; }
 
-    int64_t L = orc_seg_stride(algo, coll, P, n, ldtype);
+    int64_t L = orc_seg_stride(algo, coll, P, p_intra, n, ldtype);
     for (int q = 0; q < P; q++) {
         for (int64_t i = 0; i < nJ; i++) {
             uint64_t v;

@@ -860,3 +860,86 @@ def test_broadcast_schedule_table1(P):
             last = msgs[msgs["step"] == spl - 1]
             assert sorted(zip(last["src"].tolist(), last["dst"].tolist())) == \
                 [(2 * i + par, 2 * i + 1 - par) for i in range(r)]
+
+
+# ---------------------------------------------------------------------------
+# plain hierarchical AllReduce: intra-server RS (mesh) -> inter-server RHD AR
+# -> intra-server AG (mesh)
+# ---------------------------------------------------------------------------
+HIER_SHAPES = [(1, 1), (4, 1), (4, 4), (6, 3), (8, 2), (8, 4), (12, 4), (12, 2), (15, 3),
+               (20, 4), (24, 8), (32, 8), (40, 8), (64, 8)]
+
+
+def hier_tree(P, pin, k):
+    pout = P // pin
+    pp = 1 << (pout.bit_length() - 1)
+    r = pout - pp
+    l = k // pp
+    I = [chain([s * pin + (l + j) % pin for j in range(pin)]) for s in range(pout)]
+    u = [(I[2 * v], I[2 * v + 1]) if v < r else I[v + r] for v in range(pp)]
+    return balanced(u)
+
+
+@pytest.mark.parametrize("P,pin", HIER_SHAPES)
+def test_hier_definition_contributions_and_trees(P, pin):
+    S = O.num_segments("hier", "allreduce", P, pin)
+    n = 4 * S + 3
+    for op in ("sum", "prod", "max", "min"):
+        X = hc_inputs.uniform_int32(P, n, seed=P + pin)
+        if op == "prod":
+            X = (X % 5).astype(np.int32)
+        Y = O.replay("hier", "allreduce", X, op, "int32", p_intra=pin)
+        want = np_definition(X, op, "int32")
+        assert all(np.array_equal(Y[r], want) for r in range(P))
+    O.sym_reset()
+    Ys = O.replay_sym("hier", "allreduce", P, n, p_intra=pin)
+    segs = O.segments("hier", "allreduce", P, n, "float32", p_intra=pin)
+    for k, (off, ln) in enumerate(segs):
+        if ln == 0:
+            continue
+        for r in range(P):
+            cnt = O.sym_leaves(Ys[r, off])
+            assert np.all(cnt[:P] == 1) and cnt[P:].sum() == 0
+        assert canon(parse_expr(O.sym_string(Ys[0, off]))) == canon(hier_tree(P, pin, k))
+    rng = np.random.default_rng(P)
+    Xf = (rng.standard_normal((P, n)) * np.exp2(rng.integers(-12, 12, (P, n)))).astype(np.float32)
+    Yf = O.replay("hier", "allreduce", Xf, "sum", "float32", p_intra=pin)
+    for k, (off, ln) in enumerate(segs):
+        if ln == 0:
+            continue
+        want = eval_tree(hier_tree(P, pin, k), lambda i: Xf[i, off:off + ln], lambda a, b: a + b)
+        np.testing.assert_array_equal(Yf[0, off:off + ln].view(np.uint32),
+                                      np.asarray(want, np.float32).view(np.uint32))
+
+
+@pytest.mark.parametrize("P,pin", HIER_SHAPES)
+def test_hier_steps_and_traffic(P, pin):
+    """One intra-server mesh step, then the RHD AllReduce over servers
+    (2 ceil(log2 p_inter) steps, Table 1 of the RHD article), then one mesh
+    step.  Traffic per rank for a power-of-two server count:
+    (p_intra - 1) n / p_intra twice (mesh RS and mesh AG) plus the RHD
+    AllReduce of the intra segment, 2 (p_inter - 1) / p_inter n / p_intra."""
+    pout = P // pin
+    S = O.num_segments("hier", "allreduce", P, pin)
+    n = 16 * S
+    msgs, spl, _ = O.schedule("hier", "allreduce", P, n, p_intra=pin)
+    want_steps = (2 if pin > 1 else 0) + (2 * math.ceil(math.log2(pout)) if pout > 1 else 0)
+    assert spl == want_steps
+    if pout & (pout - 1) == 0:
+        sent = bytes_sent(msgs, P)
+        seg = n // pin
+        assert np.all(sent == 2 * (pin - 1) * seg + 2 * (pout - 1) * seg // pout)
+    # the intra-server steps stay inside a server; the RHD steps join equal
+    # local indices of different servers
+    for s in steps_of(msgs):
+        intra = [a // pin == b // pin for a, b in zip(s["src"].tolist(), s["dst"].tolist())]
+        assert all(intra) or not any(intra)
+        if not any(intra):
+            assert all(a % pin == b % pin for a, b in zip(s["src"].tolist(), s["dst"].tolist()))
+
+
+def test_hier_rejects_other_collectives():
+    with pytest.raises(ValueError):
+        O.schedule("hier", "reducescatter", 8, 64, p_intra=4)
+    with pytest.raises(ValueError):
+        O.schedule("hier", "allreduce", 8, 64, p_intra=3)
