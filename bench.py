@@ -67,6 +67,15 @@ WORKLOADS = {
                                algo="pipeline", coll="allreduce", P=32, n=8388608,
                                dtype="float32", op="sum", mode="step", p_intra=8,
                                loop_bytes=64 << 20, scale=1e-3),
+    "hier_fp32_4x8": dict(desc="Plain hierarchical AllReduce sum (mesh RS, inter-server RHD AR, "
+                               "mesh AG), 4 servers x 8 ranks (P=32), fp32, 8,388,608 elements per "
+                               "rank, fused",
+                          algo="hier", coll="allreduce", P=32, n=8388608, dtype="float32",
+                          op="sum", mode="fused", p_intra=8, loop_bytes=0, scale=1e-3),
+    "hier_fp32_4x8_step": dict(desc="Plain hierarchical AllReduce sum, 4x8, fp32, 8,388,608 "
+                                    "elements per rank, step mode (6 launches)",
+                               algo="hier", coll="allreduce", P=32, n=8388608, dtype="float32",
+                               op="sum", mode="step", p_intra=8, loop_bytes=0, scale=1e-3),
     "rhd_fp32_p8_small": dict(desc="RHD AllReduce sum, P=8, fp32, 4096 elements per rank "
                                    "(latency regime, L2-resident), fused",
                               algo="rhd", coll="allreduce", P=8, n=4096, dtype="float32",
@@ -78,8 +87,9 @@ WORKLOADS = {
 }
 DTYPE_TAG = {"float32": "f32", "bfloat16": "bf16", "int32": "int32"}
 ESIZE = {"float32": 4, "bfloat16": 2, "int32": 4}
-KERNEL_FILE = os.path.join(ROOT, "collective_communication_algorithms_gb300", "csrc",
-                           "hc_kernels.cu")
+KERNEL_DIR = os.path.join(ROOT, "collective_communication_algorithms_gb300", "csrc")
+KERNEL_FILES = ("hc_device.cuh", "hc_kernels.cu", "hc_fused_ring.cu", "hc_fused_rhd.cu",
+                "hc_fused_pipe.cu", "hc_fused_hier.cu")
 
 
 def parse_args():
@@ -125,8 +135,12 @@ def measured_peak():
 
 
 def kernel_source_hash():
-    with open(KERNEL_FILE, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """sha256 prefix over every device source file, in a fixed order."""
+    h = hashlib.sha256()
+    for name in KERNEL_FILES:
+        with open(os.path.join(KERNEL_DIR, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def traffic_from_profiles(workload):

@@ -15,7 +15,7 @@ MAX_RANKS = 64
 
 DTYPES = {"int32": 0, "float32": 1, "bfloat16": 2}
 OPS = {"sum": 0, "prod": 1, "max": 2, "min": 3}
-ALGOS = {"ring": 0, "rhd": 1, "pipeline": 2}
+ALGOS = {"ring": 0, "rhd": 1, "pipeline": 2, "hier": 3}
 COLLS = {"allreduce": 0, "reducescatter": 1, "allgather": 2, "broadcast": 3}
 MODES = {"fused": 0, "step": 1}
 STATUS = {0: "HC_OK", 1: "HC_ERR_INVALID_ARG", 2: "HC_ERR_UNSUPPORTED", 3: "HC_ERR_ALIGN",

@@ -16,7 +16,8 @@ CSRC = os.path.join(HERE, "csrc")
 OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libhc.so")
 ARCHIVE = os.path.join(OUT, "libhc.a")
-SOURCES = ["hc_kernels.cu", "hc_sched.cpp", "hc_api.cpp", "hc_graph.cpp", "hc_static_scratch.cu"]
+SOURCES = ["hc_kernels.cu", "hc_fused_ring.cu", "hc_fused_rhd.cu", "hc_fused_pipe.cu",
+           "hc_fused_hier.cu", "hc_sched.cpp", "hc_api.cpp", "hc_graph.cpp", "hc_static_scratch.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -50,7 +51,8 @@ def _stale(target, deps):
 def build(force: bool = False) -> str:
     os.makedirs(OUT, exist_ok=True)
     deps = [os.path.join(CSRC, s) for s in SOURCES]
-    deps += [os.path.join(CSRC, "hc_internal.h"), os.path.join(ROOT, "include", "hc.h")]
+    deps += [os.path.join(CSRC, "hc_internal.h"), os.path.join(CSRC, "hc_device.cuh"),
+             os.path.join(ROOT, "include", "hc.h")]
     if not force and not _stale(LIB, deps):
         return LIB
     objs = [os.path.join(OUT, os.path.splitext(s)[0] + ".o") for s in SOURCES]

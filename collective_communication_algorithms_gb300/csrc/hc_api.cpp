@@ -17,7 +17,9 @@ namespace {
 
 bool valid_dtype(hc_dtype_t d) { return d == HC_INT32 || d == HC_FLOAT32 || d == HC_BFLOAT16; }
 bool valid_op(hc_op_t o) { return o == HC_SUM || o == HC_PROD || o == HC_MAX || o == HC_MIN; }
-bool valid_algo(hc_algo_t a) { return a == HC_ALGO_RING || a == HC_ALGO_RHD || a == HC_ALGO_PIPELINE; }
+bool valid_algo(hc_algo_t a) {
+    return a == HC_ALGO_RING || a == HC_ALGO_RHD || a == HC_ALGO_PIPELINE || a == HC_ALGO_HIER;
+}
 bool valid_coll(hc_coll_t c) {
     return c == HC_COLL_ALLREDUCE || c == HC_COLL_REDUCE_SCATTER || c == HC_COLL_ALLGATHER ||
            c == HC_COLL_BROADCAST;
@@ -37,7 +39,7 @@ hc_status_t read_opts(const hc_opts_t* o, hc_algo_t algo, int P, Opts* out) {
     if (o->struct_size < sizeof(hc_opts_t)) return HC_ERR_INVALID_ARG;
     if (o->mode != HC_MODE_FUSED && o->mode != HC_MODE_STEP) return HC_ERR_INVALID_ARG;
     out->mode = o->mode;
-    if (algo == HC_ALGO_PIPELINE) {
+    if (algo == HC_ALGO_PIPELINE || algo == HC_ALGO_HIER) {
         if (o->ranks_per_server < 1 || P % o->ranks_per_server) return HC_ERR_INVALID_ARG;
         out->p_intra = o->ranks_per_server;
     }
@@ -127,6 +129,7 @@ hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, 
     const bool bcast = coll == HC_COLL_BROADCAST;
     if (bcast && (root < 0 || root >= P)) return HC_ERR_INVALID_ARG;
     if (bcast && algo != HC_ALGO_RHD) return HC_ERR_UNSUPPORTED;
+    if (algo == HC_ALGO_HIER && coll != HC_COLL_ALLREDUCE) return HC_ERR_UNSUPPORTED;
     Opts o;
     hc_status_t st = read_opts(opts, algo, P, &o);
     if (st != HC_OK) return st;
@@ -149,7 +152,7 @@ hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, 
 
     const int64_t n = (int64_t)count;
     const int es = elem_bytes(dtype);
-    c.lay = make_layout(algo, coll, P, n, dtype);
+    c.lay = make_layout(algo, coll, P, n, dtype, o.p_intra);
     const Layout& own = c.lay;  // the per-rank segment of RS / AG is the rank's own
 
     // a buffer of zero elements (the ReduceScatter output or AllGather input
@@ -376,6 +379,7 @@ hc_status_t hc_allgather(const void* const* send, void* const* recv, int P, size
 
 int hc_num_segments(hc_algo_t algo, hc_coll_t coll, int P) {
     if (!valid_algo(algo) || !valid_coll(coll) || P < 1 || P > kMaxRanks) return 0;
+    if (algo == HC_ALGO_HIER) return 0;  // depends on ranks_per_server
     return num_segments(algo, coll, P);
 }
 
@@ -384,6 +388,7 @@ hc_status_t hc_segment_range(hc_algo_t algo, hc_coll_t coll, int P, size_t count
     if (!valid_algo(algo) || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
     if (P < 1 || P > kMaxRanks || !off || !len) return HC_ERR_INVALID_ARG;
     if (count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
+    if (algo == HC_ALGO_HIER) return HC_ERR_UNSUPPORTED;
     Layout lay = make_layout(algo, coll, P, (int64_t)count, dtype);
     if (k < 0 || k >= lay.S) return HC_ERR_INVALID_ARG;
     *off = (size_t)lay.seg_lo(k);
@@ -402,7 +407,7 @@ hc_status_t hc_schedule_stats(hc_algo_t algo, hc_coll_t coll, int P, int ranks_p
     if (!valid_algo(algo) || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
     if (P < 1 || P > kMaxRanks || count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
     if (stats && stats->struct_size < sizeof(hc_stats_t)) return HC_ERR_INVALID_ARG;
-    int p_intra = algo == HC_ALGO_PIPELINE ? ranks_per_server : 1;
+    int p_intra = (algo == HC_ALGO_PIPELINE || algo == HC_ALGO_HIER) ? ranks_per_server : 1;
     if (p_intra < 1 || P % p_intra) return HC_ERR_INVALID_ARG;
     const int64_t n = (int64_t)count;
     int spl = 0;
@@ -446,7 +451,7 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
     if (!valid_algo(algo) || !valid_coll(coll) || !valid_dtype(dtype) || !n_out)
         return HC_ERR_INVALID_ARG;
     if (P < 1 || P > kMaxRanks || count > (size_t)INT64_MAX / 16) return HC_ERR_INVALID_ARG;
-    int p_intra = algo == HC_ALGO_PIPELINE ? ranks_per_server : 1;
+    int p_intra = (algo == HC_ALGO_PIPELINE || algo == HC_ALGO_HIER) ? ranks_per_server : 1;
     if (p_intra < 1 || P % p_intra) return HC_ERR_INVALID_ARG;
     Aliasing al;
     for (int r = 0; r < P; r++) {

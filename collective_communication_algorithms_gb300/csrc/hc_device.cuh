@@ -1,0 +1,370 @@
+// hc_device.cuh -- device-side building blocks shared by the kernel
+// translation units of libhc: the element-wise operators (int32 wrap, fp32
+// RNE without contraction or flush to zero, bf16 widened to fp32 and rounded
+// back with cvt.rn.bf16x2.f32, max/min by IEEE totalOrder keys), 16-byte
+// memory access, and the fused register-path kernel template with the
+// association order of every schedule.  Internal; not installed.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "hc_internal.h"
+
+namespace hc {
+
+struct FusedParams {
+    uintptr_t src[kMaxRanks];  // global-indexed input view of each rank
+    uintptr_t dst[kMaxRanks];  // global-indexed output view of each rank
+    int64_t L;
+    int64_t n;
+    int P;
+    int p_intra;
+    int pp;                    // RHD: power-of-two core size
+    int rfold;                 // RHD: number of folded pairs
+    int stages;                // TMA kernels: pipeline depth
+    int owner;                 // Broadcast: the root owns the single segment (-1: segment k's owner is k)
+    unsigned long long skip_mask;  // AllGather / Broadcast: ranks whose data is already in place
+};
+
+// Register-path fused kernels, one translation unit per algorithm.
+// coll: 0 AllReduce, 1 ReduceScatter; V: vectors per thread (1, or 2 where
+// provided).  Returns nullptr for a combination that is not provided.
+void* pick_fused_ring(int coll, hc_dtype_t dt, hc_op_t op, int V);
+// large: P >= 16 (power-of-two core of 16 or more ranks)
+void* pick_fused_rhd(int coll, hc_dtype_t dt, hc_op_t op, int V, bool large);
+void* pick_fused_pipe(int coll, hc_dtype_t dt, hc_op_t op, int V);
+void* pick_fused_hier(int coll, hc_dtype_t dt, hc_op_t op, int V);
+
+namespace {
+
+// Kernel-table tag of the RHD kernels for 16 or more ranks (pp >= 16).
+constexpr hc_algo_t kAlgoRhdLarge = (hc_algo_t)100;
+
+
+// ---------------------------------------------------------------------------
+// element-wise operators on 32-bit words (one fp32/int32, or two bf16)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t key32(uint32_t u) {
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ uint32_t key16(uint32_t h) {  // h in the low 16 bits
+    return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+template <hc_dtype_t DT, hc_op_t OP>
+struct WordOp;
+
+template <hc_op_t OP>
+struct WordOp<HC_INT32, OP> {
+    __device__ __forceinline__ static uint32_t f(uint32_t a, uint32_t b) {
+        if (OP == HC_SUM) return a + b;
+        if (OP == HC_PROD) return a * b;
+        if (OP == HC_MAX) return ((int32_t)a < (int32_t)b) ? b : a;
+        return ((int32_t)b < (int32_t)a) ? b : a;
+    }
+};
+
+template <hc_op_t OP>
+struct WordOp<HC_FLOAT32, OP> {
+    __device__ __forceinline__ static uint32_t f(uint32_t a, uint32_t b) {
+        if (OP == HC_SUM) return __float_as_uint(__fadd_rn(__uint_as_float(a), __uint_as_float(b)));
+        if (OP == HC_PROD) return __float_as_uint(__fmul_rn(__uint_as_float(a), __uint_as_float(b)));
+        if (OP == HC_MAX) return key32(a) < key32(b) ? b : a;
+        return key32(b) < key32(a) ? b : a;
+    }
+};
+
+template <hc_op_t OP>
+struct WordOp<HC_BFLOAT16, OP> {
+    __device__ __forceinline__ static uint32_t f(uint32_t a, uint32_t b) {
+        if (OP == HC_SUM)
+            return pack_bf16x2(__fadd_rn(bf_lo(a), bf_lo(b)), __fadd_rn(bf_hi(a), bf_hi(b)));
+        if (OP == HC_PROD)
+            return pack_bf16x2(__fmul_rn(bf_lo(a), bf_lo(b)), __fmul_rn(bf_hi(a), bf_hi(b)));
+        uint32_t alo = a & 0xFFFFu, blo = b & 0xFFFFu, ahi = a >> 16, bhi = b >> 16;
+        uint32_t lo, hi;
+        if (OP == HC_MAX) {
+            lo = key16(alo) < key16(blo) ? blo : alo;
+            hi = key16(ahi) < key16(bhi) ? bhi : ahi;
+        } else {
+            lo = key16(blo) < key16(alo) ? blo : alo;
+            hi = key16(bhi) < key16(ahi) ? bhi : ahi;
+        }
+        return lo | (hi << 16);
+    }
+};
+
+template <hc_dtype_t DT, hc_op_t OP>
+__device__ __forceinline__ uint4 vop(const uint4& a, const uint4& b) {
+    using W = WordOp<DT, OP>;
+    return make_uint4(W::f(a.x, b.x), W::f(a.y, b.y), W::f(a.z, b.z), W::f(a.w, b.w));
+}
+template <hc_dtype_t DT, hc_op_t OP>
+__device__ __forceinline__ uint32_t vop(uint32_t a, uint32_t b) {
+    return WordOp<DT, OP>::f(a, b);
+}
+
+// ---------------------------------------------------------------------------
+// memory access: 16-byte vectors, or one element (ragged end of a vector)
+// ---------------------------------------------------------------------------
+template <int ES>
+__device__ __forceinline__ uint32_t ld_elem(uintptr_t p) {
+    if (ES == 2) return *(const uint16_t*)p;
+    return *(const uint32_t*)p;
+}
+template <int ES>
+__device__ __forceinline__ void st_elem(uintptr_t p, uint32_t v) {
+    if (ES == 2) *(uint16_t*)p = (uint16_t)v;
+    else *(uint32_t*)p = v;
+}
+__device__ __forceinline__ uint4 ld_vec(uintptr_t p) { return *(const uint4*)p; }
+__device__ __forceinline__ void st_vec(uintptr_t p, const uint4& v) { *(uint4*)p = v; }
+// streaming variants for data touched once by the fused kernels
+__device__ __forceinline__ uint4 ld_stream(uintptr_t p) { return __ldcs((const uint4*)p); }
+__device__ __forceinline__ void st_stream(uintptr_t p, const uint4& v) { __stcs((uint4*)p, v); }
+
+template <hc_dtype_t DT>
+struct DT_ {
+    static constexpr int ES = DT == HC_BFLOAT16 ? 2 : 4;
+    static constexpr int A = 16 / ES;
+};
+
+// ---------------------------------------------------------------------------
+// fused kernels
+// ---------------------------------------------------------------------------
+
+
+constexpr int kFusedThreads = 256;
+constexpr int kBatch = 8;
+
+// V 16-byte vectors handled together by one thread (more loads in flight)
+template <int V>
+struct VecN {
+    uint4 v[V];
+};
+template <hc_dtype_t DT, hc_op_t OP, int V>
+__device__ __forceinline__ VecN<V> vop(const VecN<V>& a, const VecN<V>& b) {
+    VecN<V> r;
+#pragma unroll
+    for (int j = 0; j < V; j++) r.v[j] = vop<DT, OP>(a.v[j], b.v[j]);
+    return r;
+}
+
+// Reduce a chain x_0 (+) x_1 (+) ... (+) x_{cnt-1}, x_i = load(rank(i)), with
+// loads issued kBatch at a time for memory-level parallelism.
+template <hc_dtype_t DT, hc_op_t OP, class V, class Load>
+__device__ __forceinline__ V chain_reduce(int cnt, int base, int rot, int mod, Load load) {
+    int r = rot;
+    V acc = load(base + r);
+    int i = 1;
+    for (; i + kBatch <= cnt; i += kBatch) {
+        V x[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; j++) {
+            if (++r == mod) r = 0;
+            x[j] = load(base + r);
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; j++) acc = vop<DT, OP>(acc, x[j]);
+    }
+    for (; i < cnt; i++) {
+        if (++r == mod) r = 0;
+        acc = vop<DT, OP>(acc, load(base + r));
+    }
+    return acc;
+}
+
+// Balanced pairwise tree over leaves [w0, w0 + N), N a power of two.
+template <hc_dtype_t DT, hc_op_t OP, int N, class V, class Leaf>
+__device__ __forceinline__ V tree_fixed(int w0, Leaf leaf) {
+    if constexpr (N == 1) {
+        return leaf(w0);
+    } else {
+        V a = tree_fixed<DT, OP, N / 2, V>(w0, leaf);
+        V b = tree_fixed<DT, OP, N / 2, V>(w0 + N / 2, leaf);
+        return vop<DT, OP>(a, b);
+    }
+}
+
+// Balanced pairwise tree over `count` leaves (a power of two) evaluated with
+// a runtime loop: leaf w is merged with the pending left subtrees of the
+// levels where w has a 1 bit (left operand = left subtree, exactly as the
+// recursive tree_fixed), so the leaf code is instantiated once.
+template <hc_dtype_t DT, hc_op_t OP, class V, class Leaf>
+__device__ __forceinline__ V balanced_loop(int count, Leaf leaf) {
+    V st[7];
+    for (int w = 0; w < count; w++) {
+        V x = leaf(w);
+#pragma unroll
+        for (int h = 0; h < 7; h++) {
+            if ((w >> h) & 1) {
+                x = vop<DT, OP>(st[h], x);
+            } else {
+                st[h] = x;
+                break;
+            }
+        }
+    }
+    V res = st[0];
+#pragma unroll
+    for (int h = 1; h < 7; h++)
+        if ((1 << h) == count) res = st[h];
+    return res;
+}
+
+// RHD tree: leaves u_w = X_{2w+1} (+) X_{2w} for w < rfold (the fold step:
+// rank 2w+1's data arrives at rank 2w), else X_{w + rfold}; balanced
+// pairwise tree over the pp leaves, partner bit 0 first.
+// LARGE = false: pp <= 8 (P < 16), trees unrolled at compile time, so that
+// all loads are in flight together and the kernel keeps few registers;
+// LARGE = true: pp = 16 unrolled, 32 and 64 by a runtime loop over
+// compile-time subtrees of 8 leaves (separate kernels, so the small case does
+// not pay the registers of the large ones).
+template <hc_dtype_t DT, hc_op_t OP, bool LARGE, class V, class Load>
+__device__ __forceinline__ V rhd_reduce(int pp, int rfold, Load load) {
+    auto leaf = [&](int w) -> V {
+        if (w < rfold) return vop<DT, OP>(load(2 * w + 1), load(2 * w));
+        return load(w + rfold);
+    };
+    if constexpr (!LARGE) {
+        switch (pp) {
+        case 1: return tree_fixed<DT, OP, 1, V>(0, leaf);
+        case 2: return tree_fixed<DT, OP, 2, V>(0, leaf);
+        case 4: return tree_fixed<DT, OP, 4, V>(0, leaf);
+        default: return tree_fixed<DT, OP, 8, V>(0, leaf);
+        }
+    } else {
+        if (pp == 16) return tree_fixed<DT, OP, 16, V>(0, leaf);
+        return balanced_loop<DT, OP, V>(pp / 8, [&](int g) -> V { return tree_fixed<DT, OP, 8, V>(8 * g, leaf); });
+    }
+}
+
+// The same RHD tree with a leaf that is itself a long computation (the
+// hierarchical AllReduce's intra-server chains): one runtime loop over the
+// pp leaves, so the group code is instantiated twice rather than pp times.
+template <hc_dtype_t DT, hc_op_t OP, class V, class Group>
+__device__ __forceinline__ V rhd_reduce_loop(int pp, int rfold, Group group) {
+    return balanced_loop<DT, OP, V>(pp, [&](int w) -> V {
+        return w < rfold ? vop<DT, OP>(group(2 * w + 1), group(2 * w)) : group(w + rfold);
+    });
+}
+
+// The association order of segment k for each algorithm.
+template <hc_algo_t ALGO, hc_dtype_t DT, hc_op_t OP, class V, class Load>
+__device__ __forceinline__ V segment_reduce(const FusedParams& p, int k, Load load) {
+    if constexpr (ALGO == HC_ALGO_RING) {
+        // chain X_{k+1} (+) X_{k+2} (+) ... (+) X_k
+        return chain_reduce<DT, OP, V>(p.P, 0, (k + 1) % p.P, p.P, load);
+    } else if constexpr (ALGO == HC_ALGO_RHD) {
+        return rhd_reduce<DT, OP, false, V>(p.pp, p.rfold, load);
+    } else if constexpr (ALGO == kAlgoRhdLarge) {
+        return rhd_reduce<DT, OP, true, V>(p.pp, p.rfold, load);
+    } else if constexpr (ALGO == HC_ALGO_HIER) {
+        // RHD tree over servers (pp / rfold are the server-level core size and
+        // folded pairs) whose leaves are the intra-server chains rotated from
+        // the intra segment l = k / pp
+        const int pin = p.p_intra, l = k / p.pp;
+        auto server = [&](int s) -> V { return chain_reduce<DT, OP, V>(pin, s * pin, l, pin, load); };
+        return rhd_reduce_loop<DT, OP, V>(p.pp, p.rfold, server);
+    } else {
+        // intra-server chains rotated from l, then the inter-server chain from s+1
+        const int pin = p.p_intra, pout = p.P / p.p_intra;
+        const int s = k / pin, l = k % pin;
+        int t = s + 1 == pout ? 0 : s + 1;
+        V acc = chain_reduce<DT, OP, V>(pin, t * pin, l, pin, load);
+        for (int i = 1; i < pout; i++) {
+            if (++t == pout) t = 0;
+            acc = vop<DT, OP>(acc, chain_reduce<DT, OP, V>(pin, t * pin, l, pin, load));
+        }
+        return acc;
+    }
+}
+
+// Ragged end of segment k: the fewer than A elements after its last full
+// vector, element by element (one thread).
+template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP>
+__device__ void ragged_tail(const FusedParams& p, int k, int64_t from, int64_t to) {
+    constexpr int ES = DT_<DT>::ES;
+    for (int64_t x = from; x < to; x++) {
+        const uintptr_t xo = (uintptr_t)x * ES;
+        auto load = [&](int r) -> uint32_t { return ld_elem<ES>(p.src[r] + xo); };
+        uint32_t acc = segment_reduce<ALGO, DT, OP, uint32_t>(p, k, load);
+        if (COLL == 0) {
+            for (int r = 0; r < p.P; r++) st_elem<ES>(p.dst[r] + xo, acc);
+        } else {
+            st_elem<ES>(p.dst[k] + xo, acc);
+        }
+    }
+}
+
+// AllReduce (COLL = 0) and ReduceScatter (COLL = 1), register path: every
+// thread loads V vectors of a segment from every rank straight into
+// registers.  grid.y = segment.
+template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP, int V>
+__global__ void __launch_bounds__(kFusedThreads)
+fused_reduce(const __grid_constant__ FusedParams p) {
+    constexpr int ES = DT_<DT>::ES;
+    constexpr int A = DT_<DT>::A;
+    const int k = blockIdx.y;
+    const int64_t sbeg = (int64_t)k * p.L;
+    if (sbeg >= p.n) return;
+    const int64_t send_ = (sbeg + p.L < p.n) ? sbeg + p.L : p.n;
+    const int64_t nfull = (send_ - sbeg) / A;
+    const int64_t chunk = (int64_t)V * blockDim.x;
+    for (int64_t base = (int64_t)blockIdx.x * chunk; base < nfull; base += (int64_t)gridDim.x * chunk) {
+        auto load = [&](int r) -> VecN<V> {
+            VecN<V> x;
+#pragma unroll
+            for (int j = 0; j < V; j++) {
+                const int64_t v = base + threadIdx.x + (int64_t)j * blockDim.x;
+                x.v[j] = v < nfull ? ld_stream(p.src[r] + (uintptr_t)(sbeg + v * A) * ES)
+                                   : make_uint4(0u, 0u, 0u, 0u);
+            }
+            return x;
+        };
+        const VecN<V> acc = segment_reduce<ALGO, DT, OP, VecN<V>>(p, k, load);
+#pragma unroll
+        for (int j = 0; j < V; j++) {
+            const int64_t v = base + threadIdx.x + (int64_t)j * blockDim.x;
+            if (v >= nfull) continue;
+            const uintptr_t off = (uintptr_t)(sbeg + v * A) * ES;
+            if (COLL == 0) {
+                for (int r = 0; r < p.P; r++) st_stream(p.dst[r] + off, acc.v[j]);
+            } else {
+                st_stream(p.dst[k] + off, acc.v[j]);
+            }
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) ragged_tail<ALGO, COLL, DT, OP>(p, k, sbeg + nfull * A, send_);
+}
+
+
+// Kernel table of one algorithm: the register-path kernels for every dtype,
+// op, collective and (where instantiated) vectors per thread.
+template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, int V>
+void* pick_fused_op(hc_op_t op) {
+    switch (op) {
+    case HC_SUM: return (void*)fused_reduce<ALGO, COLL, DT, HC_SUM, V>;
+    case HC_PROD: return (void*)fused_reduce<ALGO, COLL, DT, HC_PROD, V>;
+    case HC_MAX: return (void*)fused_reduce<ALGO, COLL, DT, HC_MAX, V>;
+    default: return (void*)fused_reduce<ALGO, COLL, DT, HC_MIN, V>;
+    }
+}
+template <hc_algo_t ALGO, int COLL, int V>
+void* pick_fused_dt(hc_dtype_t dt, hc_op_t op) {
+    switch (dt) {
+    case HC_INT32: return pick_fused_op<ALGO, COLL, HC_INT32, V>(op);
+    case HC_FLOAT32: return pick_fused_op<ALGO, COLL, HC_FLOAT32, V>(op);
+    default: return pick_fused_op<ALGO, COLL, HC_BFLOAT16, V>(op);
+    }
+}
+
+}  // namespace
+}  // namespace hc

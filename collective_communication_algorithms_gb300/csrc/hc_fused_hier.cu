@@ -1,0 +1,12 @@
+// hc_fused_hier.cu -- fused register-path kernels of one schedule (plain hierarchical: RHD tree over servers of intra-server chains):
+// AllReduce only, 1 vector per thread.  One translation unit per schedule keeps each compile short.
+#include "hc_device.cuh"
+
+namespace hc {
+
+void* pick_fused_hier(int coll, hc_dtype_t dt, hc_op_t op, int V) {
+    if (V != 1 || coll != 0) return nullptr;
+    return pick_fused_dt<HC_ALGO_HIER, 0, 1>(dt, op);
+}
+
+}  // namespace hc

@@ -39,8 +39,8 @@ struct Layout {
     int64_t seg_hi(int k) const { int64_t v = (int64_t)(k + 1) * L; return v < n ? v : n; }
 };
 
-int num_segments(hc_algo_t algo, hc_coll_t coll, int P);
-Layout make_layout(hc_algo_t algo, hc_coll_t coll, int P, int64_t n, hc_dtype_t dt);
+int num_segments(hc_algo_t algo, hc_coll_t coll, int P, int p_intra = 1);
+Layout make_layout(hc_algo_t algo, hc_coll_t coll, int P, int64_t n, hc_dtype_t dt, int p_intra = 1);
 
 struct Slicing {
     int64_t chunk = 0;  // elements per segment per loop

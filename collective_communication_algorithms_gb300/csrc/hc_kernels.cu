@@ -25,105 +25,10 @@
 #include <algorithm>
 #include <cstring>
 
-#include "hc_internal.h"
+#include "hc_device.cuh"
 
 namespace hc {
 namespace {
-
-// ---------------------------------------------------------------------------
-// element-wise operators on 32-bit words (one fp32/int32, or two bf16)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t key32(uint32_t u) {
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ uint32_t key16(uint32_t h) {  // h in the low 16 bits
-    return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
-}
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    uint32_t d;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
-    return d;
-}
-__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-template <hc_dtype_t DT, hc_op_t OP>
-struct WordOp;
-
-template <hc_op_t OP>
-struct WordOp<HC_INT32, OP> {
-    __device__ __forceinline__ static uint32_t f(uint32_t a, uint32_t b) {
-        if (OP == HC_SUM) return a + b;
-        if (OP == HC_PROD) return a * b;
-        if (OP == HC_MAX) return ((int32_t)a < (int32_t)b) ? b : a;
-        return ((int32_t)b < (int32_t)a) ? b : a;
-    }
-};
-
-template <hc_op_t OP>
-struct WordOp<HC_FLOAT32, OP> {
-    __device__ __forceinline__ static uint32_t f(uint32_t a, uint32_t b) {
-        if (OP == HC_SUM) return __float_as_uint(__fadd_rn(__uint_as_float(a), __uint_as_float(b)));
-        if (OP == HC_PROD) return __float_as_uint(__fmul_rn(__uint_as_float(a), __uint_as_float(b)));
-        if (OP == HC_MAX) return key32(a) < key32(b) ? b : a;
-        return key32(b) < key32(a) ? b : a;
-    }
-};
-
-template <hc_op_t OP>
-struct WordOp<HC_BFLOAT16, OP> {
-    __device__ __forceinline__ static uint32_t f(uint32_t a, uint32_t b) {
-        if (OP == HC_SUM)
-            return pack_bf16x2(__fadd_rn(bf_lo(a), bf_lo(b)), __fadd_rn(bf_hi(a), bf_hi(b)));
-        if (OP == HC_PROD)
-            return pack_bf16x2(__fmul_rn(bf_lo(a), bf_lo(b)), __fmul_rn(bf_hi(a), bf_hi(b)));
-        uint32_t alo = a & 0xFFFFu, blo = b & 0xFFFFu, ahi = a >> 16, bhi = b >> 16;
-        uint32_t lo, hi;
-        if (OP == HC_MAX) {
-            lo = key16(alo) < key16(blo) ? blo : alo;
-            hi = key16(ahi) < key16(bhi) ? bhi : ahi;
-        } else {
-            lo = key16(blo) < key16(alo) ? blo : alo;
-            hi = key16(bhi) < key16(ahi) ? bhi : ahi;
-        }
-        return lo | (hi << 16);
-    }
-};
-
-template <hc_dtype_t DT, hc_op_t OP>
-__device__ __forceinline__ uint4 vop(const uint4& a, const uint4& b) {
-    using W = WordOp<DT, OP>;
-    return make_uint4(W::f(a.x, b.x), W::f(a.y, b.y), W::f(a.z, b.z), W::f(a.w, b.w));
-}
-template <hc_dtype_t DT, hc_op_t OP>
-__device__ __forceinline__ uint32_t vop(uint32_t a, uint32_t b) {
-    return WordOp<DT, OP>::f(a, b);
-}
-
-// ---------------------------------------------------------------------------
-// memory access: 16-byte vectors, or one element (ragged end of a vector)
-// ---------------------------------------------------------------------------
-template <int ES>
-__device__ __forceinline__ uint32_t ld_elem(uintptr_t p) {
-    if (ES == 2) return *(const uint16_t*)p;
-    return *(const uint32_t*)p;
-}
-template <int ES>
-__device__ __forceinline__ void st_elem(uintptr_t p, uint32_t v) {
-    if (ES == 2) *(uint16_t*)p = (uint16_t)v;
-    else *(uint32_t*)p = v;
-}
-__device__ __forceinline__ uint4 ld_vec(uintptr_t p) { return *(const uint4*)p; }
-__device__ __forceinline__ void st_vec(uintptr_t p, const uint4& v) { *(uint4*)p = v; }
-// streaming variants for data touched once by the fused kernels
-__device__ __forceinline__ uint4 ld_stream(uintptr_t p) { return __ldcs((const uint4*)p); }
-__device__ __forceinline__ void st_stream(uintptr_t p, const uint4& v) { __stcs((uint4*)p, v); }
-
-template <hc_dtype_t DT>
-struct DT_ {
-    static constexpr int ES = DT == HC_BFLOAT16 ? 2 : 4;
-    static constexpr int A = 16 / ES;
-};
 
 // ---------------------------------------------------------------------------
 // step kernel
@@ -188,187 +93,6 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
             }
         }
     }
-}
-
-// ---------------------------------------------------------------------------
-// fused kernels
-// ---------------------------------------------------------------------------
-struct FusedParams {
-    uintptr_t src[kMaxRanks];  // global-indexed input view of each rank
-    uintptr_t dst[kMaxRanks];  // global-indexed output view of each rank
-    int64_t L;
-    int64_t n;
-    int P;
-    int p_intra;
-    int pp;                    // RHD: power-of-two core size
-    int rfold;                 // RHD: number of folded pairs
-    int stages;                // TMA kernels: pipeline depth
-    int owner;                 // Broadcast: the root owns the single segment (-1: segment k's owner is k)
-    unsigned long long skip_mask;  // AllGather / Broadcast: ranks whose data is already in place
-};
-
-constexpr int kFusedThreads = 256;
-constexpr int kBatch = 8;
-
-// V 16-byte vectors handled together by one thread (more loads in flight)
-template <int V>
-struct VecN {
-    uint4 v[V];
-};
-template <hc_dtype_t DT, hc_op_t OP, int V>
-__device__ __forceinline__ VecN<V> vop(const VecN<V>& a, const VecN<V>& b) {
-    VecN<V> r;
-#pragma unroll
-    for (int j = 0; j < V; j++) r.v[j] = vop<DT, OP>(a.v[j], b.v[j]);
-    return r;
-}
-
-// Reduce a chain x_0 (+) x_1 (+) ... (+) x_{cnt-1}, x_i = load(rank(i)), with
-// loads issued kBatch at a time for memory-level parallelism.
-template <hc_dtype_t DT, hc_op_t OP, class V, class Load>
-__device__ __forceinline__ V chain_reduce(int cnt, int base, int rot, int mod, Load load) {
-    int r = rot;
-    V acc = load(base + r);
-    int i = 1;
-    for (; i + kBatch <= cnt; i += kBatch) {
-        V x[kBatch];
-#pragma unroll
-        for (int j = 0; j < kBatch; j++) {
-            if (++r == mod) r = 0;
-            x[j] = load(base + r);
-        }
-#pragma unroll
-        for (int j = 0; j < kBatch; j++) acc = vop<DT, OP>(acc, x[j]);
-    }
-    for (; i < cnt; i++) {
-        if (++r == mod) r = 0;
-        acc = vop<DT, OP>(acc, load(base + r));
-    }
-    return acc;
-}
-
-// Balanced pairwise tree over leaves [w0, w0 + N), N a power of two.
-template <hc_dtype_t DT, hc_op_t OP, int N, class V, class Leaf>
-__device__ __forceinline__ V tree_fixed(int w0, Leaf leaf) {
-    if constexpr (N == 1) {
-        return leaf(w0);
-    } else {
-        V a = tree_fixed<DT, OP, N / 2, V>(w0, leaf);
-        V b = tree_fixed<DT, OP, N / 2, V>(w0 + N / 2, leaf);
-        return vop<DT, OP>(a, b);
-    }
-}
-
-// RHD tree: leaves u_w = X_{2w+1} (+) X_{2w} for w < rfold (the fold step:
-// rank 2w+1's data arrives at rank 2w), else X_{w + rfold}; balanced
-// pairwise tree over the pp leaves, partner bit 0 first.
-template <hc_dtype_t DT, hc_op_t OP, class V, class Load>
-__device__ __forceinline__ V rhd_reduce(int pp, int rfold, Load load) {
-    auto leaf = [&](int w) -> V {
-        if (w < rfold) return vop<DT, OP>(load(2 * w + 1), load(2 * w));
-        return load(w + rfold);
-    };
-    switch (pp) {
-    case 1: return tree_fixed<DT, OP, 1, V>(0, leaf);
-    case 2: return tree_fixed<DT, OP, 2, V>(0, leaf);
-    case 4: return tree_fixed<DT, OP, 4, V>(0, leaf);
-    default: break;
-    }
-    // pp >= 8: subtrees of 8 leaves combined pairwise as soon as both halves
-    // exist (same tree, fewer live registers)
-    V t0 = tree_fixed<DT, OP, 8, V>(0, leaf);
-    if (pp == 8) return t0;
-    t0 = vop<DT, OP>(t0, tree_fixed<DT, OP, 8, V>(8, leaf));
-    if (pp == 16) return t0;
-    V t1 = tree_fixed<DT, OP, 8, V>(16, leaf);
-    t1 = vop<DT, OP>(t1, tree_fixed<DT, OP, 8, V>(24, leaf));
-    t0 = vop<DT, OP>(t0, t1);
-    if (pp == 32) return t0;
-    V t2 = tree_fixed<DT, OP, 8, V>(32, leaf);
-    t2 = vop<DT, OP>(t2, tree_fixed<DT, OP, 8, V>(40, leaf));
-    V t3 = tree_fixed<DT, OP, 8, V>(48, leaf);
-    t3 = vop<DT, OP>(t3, tree_fixed<DT, OP, 8, V>(56, leaf));
-    return vop<DT, OP>(t0, vop<DT, OP>(t2, t3));
-}
-
-// The association order of segment k for each algorithm.
-template <hc_algo_t ALGO, hc_dtype_t DT, hc_op_t OP, class V, class Load>
-__device__ __forceinline__ V segment_reduce(const FusedParams& p, int k, Load load) {
-    if constexpr (ALGO == HC_ALGO_RING) {
-        // chain X_{k+1} (+) X_{k+2} (+) ... (+) X_k
-        return chain_reduce<DT, OP, V>(p.P, 0, (k + 1) % p.P, p.P, load);
-    } else if constexpr (ALGO == HC_ALGO_RHD) {
-        return rhd_reduce<DT, OP, V>(p.pp, p.rfold, load);
-    } else {
-        // intra-server chains rotated from l, then the inter-server chain from s+1
-        const int pin = p.p_intra, pout = p.P / p.p_intra;
-        const int s = k / pin, l = k % pin;
-        int t = s + 1 == pout ? 0 : s + 1;
-        V acc = chain_reduce<DT, OP, V>(pin, t * pin, l, pin, load);
-        for (int i = 1; i < pout; i++) {
-            if (++t == pout) t = 0;
-            acc = vop<DT, OP>(acc, chain_reduce<DT, OP, V>(pin, t * pin, l, pin, load));
-        }
-        return acc;
-    }
-}
-
-// Ragged end of segment k: the fewer than A elements after its last full
-// vector, element by element (one thread).
-template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP>
-__device__ void ragged_tail(const FusedParams& p, int k, int64_t from, int64_t to) {
-    constexpr int ES = DT_<DT>::ES;
-    for (int64_t x = from; x < to; x++) {
-        const uintptr_t xo = (uintptr_t)x * ES;
-        auto load = [&](int r) -> uint32_t { return ld_elem<ES>(p.src[r] + xo); };
-        uint32_t acc = segment_reduce<ALGO, DT, OP, uint32_t>(p, k, load);
-        if (COLL == 0) {
-            for (int r = 0; r < p.P; r++) st_elem<ES>(p.dst[r] + xo, acc);
-        } else {
-            st_elem<ES>(p.dst[k] + xo, acc);
-        }
-    }
-}
-
-// AllReduce (COLL = 0) and ReduceScatter (COLL = 1), register path: every
-// thread loads V vectors of a segment from every rank straight into
-// registers.  grid.y = segment.
-template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP, int V>
-__global__ void __launch_bounds__(kFusedThreads)
-fused_reduce(const __grid_constant__ FusedParams p) {
-    constexpr int ES = DT_<DT>::ES;
-    constexpr int A = DT_<DT>::A;
-    const int k = blockIdx.y;
-    const int64_t sbeg = (int64_t)k * p.L;
-    if (sbeg >= p.n) return;
-    const int64_t send_ = (sbeg + p.L < p.n) ? sbeg + p.L : p.n;
-    const int64_t nfull = (send_ - sbeg) / A;
-    const int64_t chunk = (int64_t)V * blockDim.x;
-    for (int64_t base = (int64_t)blockIdx.x * chunk; base < nfull; base += (int64_t)gridDim.x * chunk) {
-        auto load = [&](int r) -> VecN<V> {
-            VecN<V> x;
-#pragma unroll
-            for (int j = 0; j < V; j++) {
-                const int64_t v = base + threadIdx.x + (int64_t)j * blockDim.x;
-                x.v[j] = v < nfull ? ld_stream(p.src[r] + (uintptr_t)(sbeg + v * A) * ES)
-                                   : make_uint4(0u, 0u, 0u, 0u);
-            }
-            return x;
-        };
-        const VecN<V> acc = segment_reduce<ALGO, DT, OP, VecN<V>>(p, k, load);
-#pragma unroll
-        for (int j = 0; j < V; j++) {
-            const int64_t v = base + threadIdx.x + (int64_t)j * blockDim.x;
-            if (v >= nfull) continue;
-            const uintptr_t off = (uintptr_t)(sbeg + v * A) * ES;
-            if (COLL == 0) {
-                for (int r = 0; r < p.P; r++) st_stream(p.dst[r] + off, acc.v[j]);
-            } else {
-                st_stream(p.dst[k] + off, acc.v[j]);
-            }
-        }
-    }
-    if (blockIdx.x == 0 && threadIdx.x == 0) ragged_tail<ALGO, COLL, DT, OP>(p, k, sbeg + nfull * A, send_);
 }
 
 // AllGather, register path: segment k read once from its owner, written to
@@ -547,35 +271,13 @@ fused_allgather_tma(const __grid_constant__ FusedParams p) {
 // ---------------------------------------------------------------------------
 // dispatch
 // ---------------------------------------------------------------------------
-// kind: 1 / 2 vectors per thread
-template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP>
-void* pick_reduce_kind(int kind) {
-    if (kind == 2) return (void*)fused_reduce<ALGO, COLL, DT, OP, 2>;
-    return (void*)fused_reduce<ALGO, COLL, DT, OP, 1>;
-}
-template <hc_algo_t ALGO, int COLL, hc_dtype_t DT>
-void* pick_reduce_op(hc_op_t op, int kind) {
-    switch (op) {
-    case HC_SUM: return pick_reduce_kind<ALGO, COLL, DT, HC_SUM>(kind);
-    case HC_PROD: return pick_reduce_kind<ALGO, COLL, DT, HC_PROD>(kind);
-    case HC_MAX: return pick_reduce_kind<ALGO, COLL, DT, HC_MAX>(kind);
-    default: return pick_reduce_kind<ALGO, COLL, DT, HC_MIN>(kind);
-    }
-}
-template <hc_algo_t ALGO, int COLL>
-void* pick_reduce_dt(hc_dtype_t dt, hc_op_t op, int kind) {
-    switch (dt) {
-    case HC_INT32: return pick_reduce_op<ALGO, COLL, HC_INT32>(op, kind);
-    case HC_FLOAT32: return pick_reduce_op<ALGO, COLL, HC_FLOAT32>(op, kind);
-    default: return pick_reduce_op<ALGO, COLL, HC_BFLOAT16>(op, kind);
-    }
-}
-template <int COLL>
-void* pick_reduce(hc_algo_t algo, hc_dtype_t dt, hc_op_t op, int kind) {
+// Register-path kernel of (algo, collective, dtype, op, vectors per thread).
+void* pick_reduce(hc_algo_t algo, int coll, hc_dtype_t dt, hc_op_t op, int V, int P) {
     switch (algo) {
-    case HC_ALGO_RING: return pick_reduce_dt<HC_ALGO_RING, COLL>(dt, op, kind);
-    case HC_ALGO_RHD: return pick_reduce_dt<HC_ALGO_RHD, COLL>(dt, op, kind);
-    default: return pick_reduce_dt<HC_ALGO_PIPELINE, COLL>(dt, op, kind);
+    case HC_ALGO_RING: return pick_fused_ring(coll, dt, op, V);
+    case HC_ALGO_RHD: return pick_fused_rhd(coll, dt, op, V, P >= 16);
+    case HC_ALGO_HIER: return pick_fused_hier(coll, dt, op, V);
+    default: return pick_fused_pipe(coll, dt, op, V);
     }
 }
 
@@ -696,10 +398,12 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     p.n = lay.n;
     p.P = a.P;
     p.p_intra = a.p_intra;
+    // RHD core: over ranks, or over servers for the hierarchical AllReduce
+    const int groups = a.algo == HC_ALGO_HIER ? a.P / a.p_intra : a.P;
     int pp = 1;
-    while (pp * 2 <= a.P) pp *= 2;
+    while (pp * 2 <= groups) pp *= 2;
     p.pp = pp;
-    p.rfold = a.P - pp;
+    p.rfold = groups - pp;
     const int S = lay.S;
     const int64_t seg_bytes = lay.L * es;
     void* args[] = {&p};
@@ -729,25 +433,33 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     // Register path.  Launch shape (vectors per thread V, blocks of 256
     // threads per SM) chosen from measurements on GB300 (fraction of the
     // measured copy bandwidth, reproducible to 0.5 % across processes):
-    //  ReduceScatter, or more than 16 ranks        V1, 8 per SM (0.92 - 0.94)
-    //  AllReduce, 4-byte types                     V1, 6 per SM (0.95)
-    //  AllReduce, bf16 max / min                   V1, 6 per SM (0.87)
-    //  AllReduce, bf16 sum / prod, RHD             V2, 6 per SM (0.97)
-    //  AllReduce, bf16 sum / prod, Ring / Pipeline V1, 4 per SM (0.95)
+    //  ReduceScatter, or more than 16 ranks         V1, 8 per SM (0.93 - 0.94)
+    //  hierarchical AllReduce                       V1, 7 per SM (0.90)
+    //  AllReduce, 4-byte types                      V1, 6 per SM (0.95)
+    //  AllReduce, bf16 max / min                    V1, 4 per SM (0.91)
+    //  AllReduce, bf16 sum / prod, RHD              V2, 3 per SM (0.98)
+    //  AllReduce, bf16 sum / prod, Ring / Pipeline  V1, 5 per SM (0.97)
     int V = 1, per_sm = 8;
-    if (COLL == 0 && a.P <= 16) {
+    if (COLL == 0 && a.algo == HC_ALGO_HIER) {
+        per_sm = 7;
+    } else if (COLL == 0 && a.P <= 16) {
         if (es == 4) {
             per_sm = 6;
         } else if (a.op == HC_MAX || a.op == HC_MIN) {
-            per_sm = 6;
+            per_sm = 4;
         } else if (a.algo == HC_ALGO_RHD) {
             V = 2;
-            per_sm = 6;
+            per_sm = 3;
         } else {
-            per_sm = 4;
+            per_sm = 5;
         }
     }
-    void* fn = COLL == 0 ? pick_reduce<0>(a.algo, a.dtype, a.op, V) : pick_reduce<1>(a.algo, a.dtype, a.op, V);
+    void* fn = pick_reduce(a.algo, COLL, a.dtype, a.op, V, a.P);
+    if (!fn && V != 1) {  // shape not instantiated: one vector per thread
+        V = 1;
+        fn = pick_reduce(a.algo, COLL, a.dtype, a.op, V, a.P);
+    }
+    if (!fn) return cudaErrorInvalidValue;
     const int64_t vecs = (lay.L + lay.A - 1) / lay.A;
     const int64_t want = std::max<int64_t>(1, (vecs + (int64_t)V * kFusedThreads - 1) / ((int64_t)V * kFusedThreads));
     const int gx = (int)std::min(want, std::max<int64_t>(1, (int64_t)sm_count * per_sm / S));

@@ -327,9 +327,117 @@ void rhd_bcast_steps(int P, int root, std::vector<LStep>& st) {
     }
 }
 
+// ---------------------------------------------------------------- hierarchical
+// Plain hierarchical AllReduce: mesh ReduceScatter inside each server, RHD
+// AllReduce among equal local indices across servers on intra segment l
+// (segments l*p' .. l*p' + p' - 1), mesh AllGather inside each server.
+void hier_steps(int P, int pin, std::vector<LStep>& st) {
+    const int pout = P / pin;
+    const int pp = core_size(pout);
+    const int r = pout - pp;
+    auto sv = [r](int v) { return v < r ? 2 * v : v + r; };  // virtual -> real server
+    auto intra_seg = [pp](int l) { return seg_range(l * pp, (l + 1) * pp); };
+    if (pin > 1) {
+        LStep x;
+        for (int s = 0; s < pout; s++)
+            for (int l = 0; l < pin; l++) {
+                LItem it;
+                it.outs = one(s * pin + l);
+                it.ins = rotation(s * pin, l, pin, pin);
+                it.segs = intra_seg(l);
+                x.push_back(it);
+            }
+        st.push_back(x);
+    }
+    if (r) {
+        LStep x;
+        for (int l = 0; l < pin; l++)
+            for (int i = 0; i < r; i++) {
+                LItem it;
+                it.outs = one(2 * i * pin + l);
+                it.acc = (2 * i + 1) * pin + l;
+                it.ins = one(2 * i * pin + l);
+                it.segs = intra_seg(l);
+                x.push_back(it);
+            }
+        st.push_back(x);
+    }
+    std::vector<int> wlo(pp, 0), whi(pp, pp);
+    for (int d = 1; d < pp; d <<= 1) {
+        LStep x;
+        std::vector<int> nlo(pp), nhi(pp);
+        for (int v = 0; v < pp; v++) {
+            const int u = v ^ d, mid = (wlo[v] + whi[v]) / 2;
+            const bool low = (v & d) == 0;
+            const int glo = low ? mid : wlo[v], ghi = low ? whi[v] : mid;
+            nlo[v] = low ? wlo[v] : mid;
+            nhi[v] = low ? mid : whi[v];
+            for (int l = 0; l < pin; l++) {
+                LItem it;
+                it.outs = one(sv(u) * pin + l);
+                it.acc = sv(v) * pin + l;
+                it.ins = one(sv(u) * pin + l);
+                it.segs = seg_range(l * pp + glo, l * pp + ghi);
+                x.push_back(it);
+            }
+        }
+        wlo = nlo;
+        whi = nhi;
+        st.push_back(x);
+    }
+    for (int d = pp / 2; d >= 1; d >>= 1) {
+        LStep x;
+        std::vector<int> nlo(pp), nhi(pp);
+        for (int v = 0; v < pp; v++) {
+            const int u = v ^ d;
+            for (int l = 0; l < pin; l++) {
+                LItem it;
+                it.outs = one(sv(u) * pin + l);
+                it.ins = one(sv(v) * pin + l);
+                it.segs = seg_range(l * pp + wlo[v], l * pp + whi[v]);
+                x.push_back(it);
+            }
+            nlo[v] = std::min(wlo[v], wlo[u]);
+            nhi[v] = std::max(whi[v], whi[u]);
+        }
+        wlo = nlo;
+        whi = nhi;
+        st.push_back(x);
+    }
+    if (r) {
+        LStep x;
+        for (int l = 0; l < pin; l++)
+            for (int i = 0; i < r; i++) {
+                LItem it;
+                it.outs = one((2 * i + 1) * pin + l);
+                it.ins = one(2 * i * pin + l);
+                it.segs = intra_seg(l);
+                x.push_back(it);
+            }
+        st.push_back(x);
+    }
+    if (pin > 1) {
+        LStep x;
+        for (int s = 0; s < pout; s++)
+            for (int l = 0; l < pin; l++) {
+                LItem it;
+                it.outs = rotation(s * pin, l + 1, pin, pin - 1);
+                it.ins = one(s * pin + l);
+                it.segs = intra_seg(l);
+                x.push_back(it);
+            }
+        st.push_back(x);
+    }
+}
+
 bool logical_steps(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root,
                    std::vector<LStep>& st) {
     st.clear();
+    if (algo == HC_ALGO_HIER) {
+        if (coll != HC_COLL_ALLREDUCE || p_intra < 1 || P % p_intra) return false;
+        hier_steps(P, p_intra, st);
+        return true;
+    }
     if (coll == HC_COLL_BROADCAST) {
         if (algo != HC_ALGO_RHD || root < 0 || root >= P) return false;
         rhd_bcast_steps(P, root, st);
@@ -398,16 +506,20 @@ DevItem make_item(const RankSet& outs, uint8_t out_loc, int acc, uint8_t acc_loc
 }  // namespace
 
 // ---------------------------------------------------------------------------
-int num_segments(hc_algo_t algo, hc_coll_t coll, int P) {
+int num_segments(hc_algo_t algo, hc_coll_t coll, int P, int p_intra) {
     if (P < 1) return 0;
     if (coll == HC_COLL_BROADCAST) return 1;
+    if (algo == HC_ALGO_HIER) {
+        if (p_intra < 1 || P % p_intra) return 0;
+        return p_intra * core_size(P / p_intra);
+    }
     if (algo == HC_ALGO_RHD && coll == HC_COLL_ALLREDUCE) return core_size(P);
     return P;
 }
 
-Layout make_layout(hc_algo_t algo, hc_coll_t coll, int P, int64_t n, hc_dtype_t dt) {
+Layout make_layout(hc_algo_t algo, hc_coll_t coll, int P, int64_t n, hc_dtype_t dt, int p_intra) {
     Layout lay;
-    lay.S = num_segments(algo, coll, P);
+    lay.S = num_segments(algo, coll, P, p_intra);
     lay.n = n;
     lay.A = kVecBytes / elem_bytes(dt);
     lay.L = (lay.S > 0 && n > 0) ? cdiv(cdiv(n, lay.S), lay.A) * lay.A : 0;
@@ -425,7 +537,7 @@ Slicing make_slicing(hc_algo_t algo, int P, int p_intra, const Layout& lay, hc_d
     const int64_t b = elem_bytes(dt);
     int64_t slots = 1;
     if (algo == HC_ALGO_RHD) slots = (P + 1) / 2;
-    else if (algo == HC_ALGO_PIPELINE) slots = std::max(1, p_intra - 1);
+    else if (algo == HC_ALGO_PIPELINE || algo == HC_ALGO_HIER) slots = std::max(1, p_intra - 1);
     const int64_t granule = 128 / b;
     int64_t c = loop_bytes / ((int64_t)P * slots * b);
     c -= c % granule;
@@ -444,7 +556,7 @@ bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root, in
     if (!logical_steps(algo, coll, P, p_intra, root, steps)) return false;
     Plan& plan = *out;
     plan = Plan();
-    plan.lay = make_layout(algo, coll, P, n, dt);
+    plan.lay = make_layout(algo, coll, P, n, dt, p_intra);
     plan.sl = make_slicing(algo, P, p_intra, plan.lay, dt, loop_bytes);
     plan.steps_per_loop = (int)steps.size();
     const int S = plan.lay.S;
@@ -553,7 +665,7 @@ bool schedule_traffic(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int ro
     std::vector<LStep> steps;
     if (P < 1 || P > kMaxRanks || !logical_steps(algo, coll, P, p_intra, root, steps)) return false;
     (void)loop_bytes;
-    Layout lay = make_layout(algo, coll, P, n, dt);
+    Layout lay = make_layout(algo, coll, P, n, dt, p_intra);
     const int b = elem_bytes(dt);
     if (steps_per_loop) *steps_per_loop = (int)steps.size();
     if (!bytes_sent) return true;

@@ -91,7 +91,20 @@ typedef enum {
 
 typedef enum { HC_INT32 = 0, HC_FLOAT32 = 1, HC_BFLOAT16 = 2 } hc_dtype_t;
 typedef enum { HC_SUM = 0, HC_PROD = 1, HC_MAX = 2, HC_MIN = 3 } hc_op_t;
-typedef enum { HC_ALGO_RING = 0, HC_ALGO_RHD = 1, HC_ALGO_PIPELINE = 2 } hc_algo_t;
+/*
+ * HC_ALGO_HIER: the plain (non-pipelined) hierarchical AllReduce of the
+ * Pipeline article's "与其它分级算法的关系" and the RHD article's
+ * "耗时模型解读": an intra-server ReduceScatter (full mesh), an inter-server
+ * RHD AllReduce among the ranks of equal local index, and an intra-server
+ * AllGather (full mesh); ranks_per_server gives the server size.  AllReduce
+ * only (the other collectives return HC_ERR_UNSUPPORTED).  Per element:
+ * intra-server chains I_s = X_(s,l) (+) X_(s,l+1) (+) ... rotated from the
+ * element's intra segment l, then the RHD tree over the servers (fold of
+ * server pairs (2i, 2i+1), balanced pairwise tree).  Its layout has
+ * ranks_per_server x 2^floor(log2 (P / ranks_per_server)) segments and is not
+ * reported by hc_segment_range.
+ */
+typedef enum { HC_ALGO_RING = 0, HC_ALGO_RHD = 1, HC_ALGO_PIPELINE = 2, HC_ALGO_HIER = 3 } hc_algo_t;
 typedef enum {
     HC_COLL_ALLREDUCE = 0,
     HC_COLL_REDUCE_SCATTER = 1,
@@ -113,13 +126,15 @@ typedef enum { HC_MODE_FUSED = 0, HC_MODE_STEP = 1 } hc_mode_t;
 /*
  * Options; pass NULL for the defaults (fused, ranks_per_server 1, one loop,
  * no scratch).  struct_size must be sizeof(hc_opts_t).
- *  ranks_per_server : Pipeline only: ranks per server (p_intra); P must be a
- *                     multiple of it; rank = server * p_intra + local.
+ *  ranks_per_server : Pipeline and hierarchical only: ranks per server
+ *                     (p_intra); P must be a multiple of it;
+ *                     rank = server * p_intra + local.
  *  max_loop_bytes   : step mode: byte limit per loop (the pages' scratch
  *                     limit maxTmpMemSize_); each segment is cut into slices
  *                     of c = align_down(max_loop_bytes / (P * slots * b),
  *                     128 / b) elements (slots = 1 Ring, ceil(P/2) RHD,
- *                     max(1, p_intra - 1) Pipeline) and the schedule runs once
+ *                     max(1, p_intra - 1) Pipeline and hierarchical) and the
+ *                     schedule runs once
  *                     per slice; 0 = one loop.  Results do not depend on it.
  *  scratch          : step mode, out-of-place ReduceScatter only: device
  *                     memory of at least hc_scratch_bytes() bytes, 16-byte

@@ -64,7 +64,7 @@ def run_collective(coll, algo, X, dtype, op="sum", mode="fused", in_place=False,
     P, n = X.shape
     if coll == "broadcast":
         return _run_broadcast(algo, X, dtype, mode, in_place, root, stream)
-    segs = segments(algo, coll, P, n, dtype)
+    segs = segments(algo, coll, P, n, dtype) if coll != "allreduce" else None
     regions = []
     send_ptrs, recv_ptrs = [], []
     scratch = None

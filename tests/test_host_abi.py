@@ -144,11 +144,11 @@ def check_races(recs, coll, in_place):
                 raise AssertionError("write/write race")
 
 
-def check_bounds(recs, algo, coll, P, n, dtype, root=None):
+def check_bounds(recs, algo, coll, P, n, dtype, root=None, p_intra=1):
     """Every record stays inside its segment (hence inside the rank vector),
     names valid ranks, and reads a rank's input (location 0) of an
     AllGather only inside that rank's own segment."""
-    segs = O.segments(algo, coll, P, n, dtype)
+    segs = O.segments(algo, coll, P, n, dtype, p_intra=p_intra)
     for r in recs:
         off, ln = segs[r["seg"]]
         assert off <= r["lo"] <= r["hi"] <= off + ln <= n
@@ -469,3 +469,60 @@ def test_broadcast_rejects_other_algorithms():
     with pytest.raises(B.HcError) as e:
         B.hc_step_plan("ring", "broadcast", 4, 100, "float32")
     assert e.value.status == 1
+
+
+HIER_SHAPES = [(1, 1), (4, 1), (4, 4), (6, 3), (8, 2), (8, 4), (12, 4), (12, 2), (15, 3),
+               (20, 4), (24, 8), (32, 8), (64, 8)]
+
+
+@pytest.mark.parametrize("P,pin", HIER_SHAPES)
+def test_hier_steps_traffic_and_plans(P, pin):
+    """Plain hierarchical AllReduce: steps and per-rank traffic equal the
+    oracle's; step plans are race-free, in bounds and, executed on the CPU,
+    give the oracle's results (in place and out of place, with loops) and its
+    association trees."""
+    S = O.num_segments("hier", "allreduce", P, pin)
+    n = 16 * S + 3
+    st, sent = B.hc_schedule_stats("hier", "allreduce", P, n, "float32", pin, 0)
+    msgs, spl, _ = O.schedule("hier", "allreduce", P, n, "float32", p_intra=pin)
+    assert st["steps_per_loop"] == spl
+    want = np.zeros(P, dtype=np.int64)
+    np.add.at(want, msgs["src"], (msgs["hi"] - msgs["lo"]) * 4)
+    assert list(want) == sent
+    for n2, lb in ((n, 0), (40 * S + 5, 2048)):
+        X = hc_inputs.uniform_int32(P, n2, seed=P + pin)
+        Y = O.replay("hier", "allreduce", X, "sum", "int32", p_intra=pin, loop_bytes=lb)
+        for in_place in (True, False):
+            recs, _ = B.hc_step_plan("hier", "allreduce", P, n2, "int32", pin, lb, in_place)
+            check_races(recs, "allreduce", in_place)
+            check_bounds(recs, "hier", "allreduce", P, n2, "int32", p_intra=pin)
+            bufs = Buffers("allreduce", X, in_place, None, fill=-7)
+            execute(recs, bufs, lambda a, b: (a + b).astype(np.int32), shuffle_seed=P)
+            for r in range(P):
+                assert np.array_equal(bufs.work[r], Y[r]), (P, pin, r, in_place, lb)
+    # association trees by symbolic execution of the plan
+    n3 = 4 * S
+    Xs = np.empty((P, n3), dtype=object)
+    for r in range(P):
+        for j in range(n3):
+            Xs[r, j] = r
+    recs, _ = B.hc_step_plan("hier", "allreduce", P, n3, "float32", pin, 0, True)
+    bufs = Buffers("allreduce", Xs, True, None, fill=None)
+
+    def combine(a, b):
+        out = np.empty(len(a), dtype=object)
+        for i in range(len(a)):
+            out[i] = (a[i], b[i])
+        return out
+    execute(recs, bufs, combine)
+    O.sym_reset()
+    Ys = O.replay_sym("hier", "allreduce", P, n3, p_intra=pin)
+    for off, ln in O.segments("hier", "allreduce", P, n3, "float32", p_intra=pin):
+        if ln:
+            assert canon(bufs.work[P - 1][off]) == canon(parse(O.sym_string(Ys[P - 1, off])))
+
+
+def test_hier_is_allreduce_only():
+    for coll in ("reducescatter", "allgather"):
+        with pytest.raises(B.HcError):
+            B.hc_step_plan("hier", coll, 8, 100, "float32", 4)
