@@ -101,8 +101,9 @@ def parse_args():
     ap.add_argument("--workload", default="ring_fp32_p8", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--sweep", choices=["small"], default=None,
-                    help="small: RHD AllReduce latency sweep (P x n), eager vs graph mode")
+    ap.add_argument("--sweep", choices=["small", "select"], default=None,
+                    help="small: RHD AllReduce latency sweep (P x n), eager vs graph mode; "
+                         "select: cost-model selector against measured times")
     return ap.parse_args()
 
 
@@ -543,10 +544,86 @@ def sweep_small(args):
             print(json.dumps(line), flush=True)
 
 
+def sweep_select(args):
+    """For each (collective, P, ranks per server, n, mode) time every
+    candidate schedule eagerly (back-to-back calls, CUDA events) and compare
+    the cost model's choice and prediction with the measured best."""
+    import torch
+    from collective_communication_algorithms_gb300 import _binding as B
+    torch.cuda.set_device(0)
+    B.lib()
+    stream = torch.cuda.current_stream()
+    sh = stream.cuda_stream
+    cases = []
+    for coll in ("allreduce", "reducescatter", "allgather"):
+        for P, rps in ((8, 1), (32, 8)):
+            for n in (4096, 262144, 4194304):
+                for mode in ("step", "fused"):
+                    cases.append((coll, P, rps, n, mode))
+    for coll, P, rps, n, mode in cases:
+        X = hc_inputs.gradients_f32(P, n, seed=0, scale=1e-3)
+        dev = torch.from_numpy(X).cuda()
+        out = torch.empty_like(dev)
+        cands = ["ring", "rhd"] + (["pipeline"] if rps > 1 else []) + \
+            (["hier"] if rps > 1 and coll == "allreduce" else [])
+        pick, pred = B.hc_select_algo(coll, P, n, "float32", mode, rps)
+        reps = 200 if n <= 262144 else 20
+        meas = {}
+        for algo in cands:
+            r_ps = rps if algo in ("pipeline", "hier") else 1
+            segs = [B.hc_segment_range(algo, coll, P, n, "float32", k) for k in range(P)] \
+                if coll != "allreduce" else None
+            send = [dev[r].data_ptr() for r in range(P)]
+            if coll == "allreduce":
+                recv = [out[r].data_ptr() for r in range(P)]
+            elif coll == "reducescatter":
+                recv = [out[r].data_ptr() for r in range(P)]
+            else:
+                send = [dev[r].data_ptr() + segs[r][0] * 4 for r in range(P)]
+                recv = [out[r].data_ptr() for r in range(P)]
+            scratch = None
+            sb = 0
+            if coll == "reducescatter" and mode == "step":
+                sb = B.hc_scratch_bytes(algo, P, n, "float32")
+                scratch = torch.empty(sb, dtype=torch.uint8, device="cuda")
+            opts = B.make_opts(mode, ranks_per_server=r_ps,
+                               scratch=scratch.data_ptr() if scratch is not None else 0,
+                               scratch_bytes=sb)
+
+            def call():
+                if coll == "allreduce":
+                    B.hc_allreduce(send, recv, P, n, "float32", "sum", algo, opts, sh)
+                elif coll == "reducescatter":
+                    B.hc_reduce_scatter(send, recv, P, n, "float32", "sum", algo, opts, sh)
+                else:
+                    B.hc_allgather(send, recv, P, n, "float32", algo, opts, sh)
+            for _ in range(5):
+                call()
+            torch.cuda.synchronize()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(reps):
+                call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            meas[algo] = e0.elapsed_time(e1) / reps * 1e3
+        best = min(meas, key=meas.get)
+        line = {"sweep": "select", "collective": coll, "P": P, "ranks_per_server": rps,
+                "elements_per_rank": n, "mode": mode, "selected": pick,
+                "predicted_us": round(pred, 2), "measured_us": {a: round(t, 2) for a, t in meas.items()},
+                "measured_best": best,
+                "selected_over_best": round(meas[pick] / meas[best], 3)}
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.sweep == "small":
         sweep_small(args)
+        return
+    if args.sweep == "select":
+        sweep_select(args)
         return
     if args.warmup < 3:
         args.warmup = 3

@@ -65,7 +65,8 @@ EXPORTS = ("hc_allreduce", "hc_reduce_scatter", "hc_reduce_scatter_static_scratc
            "hc_graph_add_broadcast", "hc_graph_build",
            "hc_graph_launch", "hc_graph_info", "hc_graph_destroy",
            "hc_num_segments", "hc_scratch_bytes", "hc_schedule_stats", "hc_step_plan",
-           "hc_device_status", "hc_last_cuda_error", "hc_status_string", "hc_version")
+           "hc_select_algo", "hc_device_status", "hc_last_cuda_error", "hc_status_string",
+           "hc_version")
 
 _lib = None
 
@@ -126,6 +127,9 @@ def lib():
                                    ctypes.POINTER(hc_plan_record_t), sz,
                                    ctypes.POINTER(sz), ctypes.POINTER(i32)]
         L.hc_step_plan.restype = i32
+        L.hc_select_algo.argtypes = [i32, i32, i32, sz, i32, i32, ctypes.POINTER(i32),
+                                     ctypes.POINTER(ctypes.c_double)]
+        L.hc_select_algo.restype = i32
         L.hc_last_cuda_error.argtypes = []
         L.hc_last_cuda_error.restype = ctypes.c_char_p
         L.hc_device_status.argtypes = [i32]
@@ -268,6 +272,16 @@ def hc_step_plan(algo, coll, P, count, dtype, ranks_per_server=1, max_loop_bytes
                     "in_ranks": list(r.in_ranks[:r.in_cnt]),
                     "out_ranks": list(r.out_ranks[:r.out_cnt])})
     return out, nl.value
+
+
+def hc_select_algo(coll, P, count, dtype, mode="step", ranks_per_server=1):
+    """(algorithm name, predicted microseconds) of the cost model."""
+    a, t = ctypes.c_int(), ctypes.c_double()
+    _check(lib().hc_select_algo(_enum(COLLS, coll), int(P), int(ranks_per_server), int(count),
+                                _enum(DTYPES, dtype), _enum(MODES, mode), ctypes.byref(a),
+                                ctypes.byref(t)), "hc_select_algo")
+    name = {v: k for k, v in ALGOS.items()}[a.value]
+    return name, t.value
 
 
 def hc_device_status(clear=True):

@@ -497,6 +497,49 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
     return HC_OK;
 }
 
+hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t count,
+                           hc_dtype_t dtype, hc_mode_t mode, hc_algo_t* out_algo,
+                           double* predicted_us) {
+    // measured on GB300 (bench.py workloads and the small-message sweep):
+    // host cost of one eager launch, device time between dependent kernels,
+    // HBM bandwidth and the fraction of it step / fused kernels reach
+    const double kHostLaunchUs = 4.6, kDeviceStepUs = 2.5;
+    const double kBandwidth = 6800e9, kStepFrac = 0.86, kFusedFrac = 0.93;
+    if (!out_algo || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
+    if (mode != HC_MODE_FUSED && mode != HC_MODE_STEP) return HC_ERR_INVALID_ARG;
+    if (P < 1 || P > kMaxRanks) return HC_ERR_INVALID_ARG;
+    std::vector<hc_algo_t> cands = {HC_ALGO_RING, HC_ALGO_RHD};
+    if (coll == HC_COLL_BROADCAST) cands = {HC_ALGO_RHD};
+    const bool servers = ranks_per_server > 1 && P % ranks_per_server == 0;
+    if (servers && coll != HC_COLL_BROADCAST) cands.push_back(HC_ALGO_PIPELINE);
+    if (servers && coll == HC_COLL_ALLREDUCE) cands.push_back(HC_ALGO_HIER);
+    double best = 0;
+    bool have = false;
+    for (hc_algo_t a : cands) {
+        hc_stats_t st;
+        std::memset(&st, 0, sizeof st);
+        st.struct_size = sizeof st;
+        const int rps = (a == HC_ALGO_PIPELINE || a == HC_ALGO_HIER) ? ranks_per_server : 1;
+        if (hc_schedule_stats(a, coll, P, rps, count, dtype, 0, &st, nullptr) != HC_OK) continue;
+        // launches are queued asynchronously: the host cost and the device
+        // time overlap, the larger one decides
+        const int launches = mode == HC_MODE_STEP ? st.launches_step : st.launches_fused;
+        const double bytes = mode == HC_MODE_STEP ? (double)st.step_bytes : (double)st.fused_bytes;
+        const double frac = mode == HC_MODE_STEP ? kStepFrac : kFusedFrac;
+        const double host = launches * kHostLaunchUs;
+        const double device = launches * kDeviceStepUs + bytes / (frac * kBandwidth) * 1e6;
+        const double t = host > device ? host : device;
+        if (!have || t < best) {
+            best = t;
+            *out_algo = a;
+            have = true;
+        }
+    }
+    if (!have) return HC_ERR_INVALID_ARG;
+    if (predicted_us) *predicted_us = best;
+    return HC_OK;
+}
+
 hc_status_t hc_device_status(int clear) {
     int v = 0;
     const hc_status_t st = cuda_status(read_device_error(clear != 0, &v));

@@ -351,6 +351,29 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
                          int* launches);
 
 /*
+ * Cost-model algorithm selection (the AllReduce article's cost model,
+ * "AllReduce算法实现": T_Ring = 2(N-1)/N M/B + 2(N-1) L, choose the
+ * cheapest; the alpha-beta-gamma tables of the RHD and Pipeline articles).
+ * On one GB300 a schedule's cost is its kernel launches (alpha) and the
+ * bytes its kernels move over the HBM bandwidth (beta; the reduction, gamma,
+ * hides under the memory traffic).  Launches are queued asynchronously, so
+ * the host's launch cost and the device time overlap:
+ *   t = max(launches * alpha_host, launches * alpha_dev + bytes / (f * B))
+ * with launches and bytes (step or fused mode) from hc_schedule_stats and
+ * alpha_host = 4.6 us per eager launch, alpha_dev = 2.5 us between dependent
+ * kernels, f = 0.86 (step) / 0.93 (fused), B = 6800 GB/s, all measured on
+ * GB300.  Candidates: Ring and RHD;
+ * Pipeline and, for an AllReduce, the hierarchical AllReduce when
+ * ranks_per_server > 1 divides P.  On a tie the earlier candidate wins (Ring,
+ * RHD, Pipeline, hierarchical).
+ *  out_algo      : the cheapest schedule
+ *  predicted_us  : its predicted time in microseconds (may be NULL)
+ */
+hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t count,
+                           hc_dtype_t dtype, hc_mode_t mode, hc_algo_t* out_algo,
+                           double* predicted_us);
+
+/*
  * Device-side status of the kernels that wait on shared-memory barriers (the
  * TMA-staged fused kernels).  Each such wait gives up after about 2 s; the
  * kernel then records HC_ERR_TIMEOUT here and returns instead of hanging.

@@ -526,3 +526,32 @@ def test_hier_is_allreduce_only():
     for coll in ("reducescatter", "allgather"):
         with pytest.raises(B.HcError):
             B.hc_step_plan("hier", coll, 8, 100, "float32", 4)
+
+
+def test_cost_model_selector():
+    """hc_select_algo: the cheapest schedule under t = max(launches * alpha_host,
+    launches * alpha_dev + bytes / (f B)), recomputed here from
+    hc_schedule_stats; small messages pick the schedule with the fewest
+    launches; the hierarchical schedule is offered only with servers."""
+    def model(algo, coll, P, n, mode, rps):
+        st, _ = B.hc_schedule_stats(algo, coll, P, n, "float32", rps, 0)
+        L = st["launches_step"] if mode == "step" else st["launches_fused"]
+        by = st["step_bytes"] if mode == "step" else st["fused_bytes"]
+        f = 0.86 if mode == "step" else 0.93
+        return max(L * 4.6, L * 2.5 + by / (f * 6800e9) * 1e6)
+    for coll in ("allreduce", "reducescatter", "allgather"):
+        for P, rps in ((2, 1), (5, 1), (8, 1), (12, 4), (16, 4), (32, 8), (64, 8)):
+            for n in (256, 4096, 1 << 20, 16 << 20):
+                for mode in ("step", "fused"):
+                    algo, t = B.hc_select_algo(coll, P, n, "float32", mode, rps)
+                    cands = ["ring", "rhd"] + (["pipeline"] if rps > 1 else []) + \
+                        (["hier"] if rps > 1 and coll == "allreduce" else [])
+                    costs = {a: model(a, coll, P, n, mode, rps if a in ("pipeline", "hier") else 1)
+                             for a in cands}
+                    assert algo in cands
+                    assert abs(t - costs[algo]) < 1e-6 * max(1, t)
+                    assert t <= min(costs.values()) + 1e-9
+    # latency regime, step mode: RHD's 2 ceil(log2 P) launches beat Ring's 2 (P - 1)
+    assert B.hc_select_algo("allreduce", 8, 1024, "float32", "step")[0] == "rhd"
+    assert B.hc_select_algo("allreduce", 16, 256, "float32", "step")[0] == "rhd"
+    assert B.hc_select_algo("broadcast", 8, 1024, "float32", "step")[0] == "rhd"
