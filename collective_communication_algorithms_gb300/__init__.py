@@ -4,9 +4,10 @@ Pipeline) for P virtual ranks whose buffers live in one GPU's memory.
 
 The work happens in libhc (include/hc.h), hand-written sm_103a kernels behind
 a C ABI.  This package is its thin Python binding: the hc_* functions mirror
-the C entry points; allreduce / reduce_scatter / allgather accept lists of
-torch CUDA tensors (one per virtual rank) and pass their pointers and the
-current CUDA stream.  PyTorch only provides device memory and streams.
+the C entry points; allreduce / reduce_scatter / allgather / broadcast accept
+lists of torch tensors (one per virtual rank: CUDA tensors, or pinned host
+tensors that the kernels then read and write over the host link) and pass
+their pointers and the current CUDA stream.  PyTorch only provides device memory and streams.
 """
 from ._binding import (ALGOS, COLLS, DTYPES, MODES, OPS, Graph, HcError, hc_allgather, hc_allreduce,
                        hc_broadcast,
@@ -39,9 +40,15 @@ def _stream(stream):
 
 def _ptrs(ts):
     for t in ts:
-        if not t.is_cuda or not t.is_contiguous():
-            raise ValueError("rank buffers must be contiguous CUDA tensors")
+        if not t.is_contiguous() or not (t.is_cuda or t.is_pinned()):
+            raise ValueError("rank buffers must be contiguous CUDA or pinned host tensors")
     return [t.data_ptr() for t in ts]
+
+
+def _on_host(*groups):
+    """True when some rank buffer is a pinned host tensor: the kernels then
+    read or write it over the host link (hc_opts_t.host_buffers)."""
+    return any(not t.is_cuda for g in groups if g is not None for t in g)
 
 
 def segment_range(algo, coll, P, count, dtype, k):
@@ -53,11 +60,11 @@ def segments(algo, coll, P, count, dtype):
             for k in range(hc_num_segments(algo, coll, P))]
 
 
-def _opts(mode, ranks_per_server, max_loop_bytes, scratch):
+def _opts(mode, ranks_per_server, max_loop_bytes, scratch, host=False):
     sp, sb = 0, 0
     if scratch is not None:
         sp, sb = scratch.data_ptr(), scratch.numel() * scratch.element_size()
-    return make_opts(mode, ranks_per_server, max_loop_bytes, sp, sb)
+    return make_opts(mode, ranks_per_server, max_loop_bytes, sp, sb, host_buffers=host)
 
 
 def allreduce(send, recv=None, op="sum", algo="ring", mode="fused", ranks_per_server=1,
@@ -66,7 +73,8 @@ def allreduce(send, recv=None, op="sum", algo="ring", mode="fused", ranks_per_se
     recv = send if recv is None else recv
     P = len(send)
     hc_allreduce(_ptrs(send), _ptrs(recv), P, send[0].numel(), _dtype_name(send[0]), op, algo,
-                 _opts(mode, ranks_per_server, max_loop_bytes, None), _stream(stream))
+                 _opts(mode, ranks_per_server, max_loop_bytes, None, _on_host(send, recv)),
+                 _stream(stream))
     return recv
 
 
@@ -75,7 +83,8 @@ def reduce_scatter(send, recv, op="sum", algo="ring", mode="fused", ranks_per_se
     """recv[r] = segment r of (+)_i send[i] (see segments())."""
     P = len(send)
     hc_reduce_scatter(_ptrs(send), _ptrs(recv), P, send[0].numel(), _dtype_name(send[0]), op,
-                      algo, _opts(mode, ranks_per_server, max_loop_bytes, scratch),
+                      algo, _opts(mode, ranks_per_server, max_loop_bytes, scratch,
+                                  _on_host(send, recv)),
                       _stream(stream))
     return recv
 
@@ -85,7 +94,8 @@ def allgather(send, recv, algo="ring", mode="fused", ranks_per_server=1, max_loo
     """recv[r][segment k] = send[k]; send=None means in place."""
     P = len(recv)
     hc_allgather(None if send is None else _ptrs(send), _ptrs(recv), P, recv[0].numel(),
-                 _dtype_name(recv[0]), algo, _opts(mode, ranks_per_server, max_loop_bytes, None),
+                 _dtype_name(recv[0]), algo,
+                 _opts(mode, ranks_per_server, max_loop_bytes, None, _on_host(send, recv)),
                  _stream(stream))
     return recv
 
@@ -94,6 +104,10 @@ def broadcast(send, recv, root=0, algo="rhd", mode="fused", stream=None):
     """recv[r] = send (the root's vector) for every rank; send=None: in place
     from recv[root]."""
     P = len(recv)
+    if send is not None:
+        _ptrs([send])
     hc_broadcast(None if send is None else send.data_ptr(), _ptrs(recv), P, recv[0].numel(),
-                 _dtype_name(recv[0]), root, algo, _opts(mode, 1, 0, None), _stream(stream))
+                 _dtype_name(recv[0]), root, algo,
+                 _opts(mode, 1, 0, None, _on_host(None if send is None else [send], recv)),
+                 _stream(stream))
     return recv

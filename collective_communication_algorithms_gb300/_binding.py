@@ -38,7 +38,8 @@ class HcError(RuntimeError):
 class hc_opts_t(ctypes.Structure):
     _fields_ = [("struct_size", ctypes.c_size_t), ("mode", ctypes.c_int),
                 ("ranks_per_server", ctypes.c_int), ("max_loop_bytes", ctypes.c_size_t),
-                ("scratch", ctypes.c_void_p), ("scratch_bytes", ctypes.c_size_t)]
+                ("scratch", ctypes.c_void_p), ("scratch_bytes", ctypes.c_size_t),
+                ("host_buffers", ctypes.c_int)]
 
 
 class hc_stats_t(ctypes.Structure):
@@ -163,7 +164,8 @@ def _ptr_array(ptrs):
     return arr
 
 
-def make_opts(mode="fused", ranks_per_server=1, max_loop_bytes=0, scratch=0, scratch_bytes=0):
+def make_opts(mode="fused", ranks_per_server=1, max_loop_bytes=0, scratch=0, scratch_bytes=0,
+              host_buffers=False):
     o = hc_opts_t()
     o.struct_size = ctypes.sizeof(hc_opts_t)
     o.mode = MODES[mode] if isinstance(mode, str) else int(mode)
@@ -171,6 +173,7 @@ def make_opts(mode="fused", ranks_per_server=1, max_loop_bytes=0, scratch=0, scr
     o.max_loop_bytes = int(max_loop_bytes)
     o.scratch = int(scratch) if scratch else None
     o.scratch_bytes = int(scratch_bytes)
+    o.host_buffers = 1 if host_buffers else 0
     return o
 
 

@@ -1,6 +1,7 @@
 // hc_api.cpp -- the C ABI of libhc (see include/hc.h): argument validation,
 // in-place detection, step-plan cache and dispatch to the kernels.
 #include <algorithm>
+#include <cstddef>
 #include <cstring>
 #include <map>
 #include <memory>
@@ -31,12 +32,18 @@ struct Opts {
     int64_t loop_bytes = 0;
     void* scratch = nullptr;
     size_t scratch_bytes = 0;
+    bool host_buffers = false;
 };
 
 hc_status_t read_opts(const hc_opts_t* o, hc_algo_t algo, int P, Opts* out) {
     *out = Opts();
     if (!o) return HC_OK;
-    if (o->struct_size < sizeof(hc_opts_t)) return HC_ERR_INVALID_ARG;
+    // callers built before host_buffers existed pass the shorter size
+    if (o->struct_size < offsetof(hc_opts_t, host_buffers)) return HC_ERR_INVALID_ARG;
+    if (o->struct_size >= sizeof(hc_opts_t)) {
+        if (o->host_buffers != 0 && o->host_buffers != 1) return HC_ERR_INVALID_ARG;
+        out->host_buffers = o->host_buffers == 1;
+    }
     if (o->mode != HC_MODE_FUSED && o->mode != HC_MODE_STEP) return HC_ERR_INVALID_ARG;
     out->mode = o->mode;
     if (algo == HC_ALGO_PIPELINE || algo == HC_ALGO_HIER) {
@@ -70,6 +77,21 @@ hc_status_t cuda_status(cudaError_t e) {
     if (e == cudaSuccess) return HC_OK;
     g_last_cuda_error = e;
     return HC_ERR_CUDA;
+}
+
+// A buffer the kernels may dereference at its own address: device or managed
+// memory, or page-locked host memory mapped at the same address (unified
+// addressing).  Pageable memory, or host memory mapped elsewhere, is refused.
+hc_status_t check_device_accessible(const void* p) {
+    cudaPointerAttributes at;
+    const cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();  // leave no pending error behind for the caller
+        return cuda_status(e);
+    }
+    if (at.type == cudaMemoryTypeDevice || at.type == cudaMemoryTypeManaged) return HC_OK;
+    if (at.type == cudaMemoryTypeHost && at.devicePointer == p) return HC_OK;
+    return HC_ERR_INVALID_ARG;
 }
 
 int sm_count_of_current_device() {
@@ -166,7 +188,12 @@ hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, 
         if ((recv_used && !recv[r]) || (send_used && !send[r])) return HC_ERR_INVALID_ARG;
         if ((recv_used && ((uintptr_t)recv[r] & 15)) || (send_used && ((uintptr_t)send[r] & 15)))
             return HC_ERR_ALIGN;
+        if (o.host_buffers) {
+            if (recv_used && (st = check_device_accessible(recv[r])) != HC_OK) return st;
+            if (send_used && (st = check_device_accessible(send[r])) != HC_OK) return st;
+        }
     }
+    c.host_buffers = o.host_buffers;
 
     std::memset(&c.al, 0, sizeof c.al);
     std::vector<Interval> iv;
@@ -288,6 +315,7 @@ hc_status_t execute(const Prepared& c, cudaStream_t stream) {
         std::memcpy(a.ag_in_place, c.ag_in_place, sizeof a.ag_in_place);
         std::memcpy(a.rs_in_place, c.rs_in_place, sizeof a.rs_in_place);
         a.root = c.root;
+        a.host_buffers = c.host_buffers;
         return cuda_status(launch_fused(a, stream, sms));
     }
     uintptr_t base[LOC_COUNT][kMaxRanks];

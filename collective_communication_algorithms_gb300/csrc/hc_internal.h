@@ -135,6 +135,7 @@ struct FusedArgs {
     bool ag_in_place[kMaxRanks];
     bool rs_in_place[kMaxRanks];
     int root;  // Broadcast root, -1 otherwise
+    bool host_buffers;  // some buffers are page-locked host memory
 };
 
 // ---------------------------------------------------------------------------
@@ -158,6 +159,7 @@ struct Prepared {
     size_t count = 0;
     bool empty = true;
     bool has_send = false;
+    bool host_buffers = false;
     Layout lay;
     Aliasing al;
     bool rs_in_place[kMaxRanks] = {false};

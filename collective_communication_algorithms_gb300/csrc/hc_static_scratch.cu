@@ -58,5 +58,6 @@ extern "C" hc_status_t hc_reduce_scatter_static_scratch(
     o.max_loop_bytes = max_loop_bytes;
     o.scratch = scratch;
     o.scratch_bytes = HC_STATIC_SCRATCH_BYTES;
+    o.host_buffers = 0;
     return hc_reduce_scatter(send, recv, P, count, dtype, op, algo, &o, stream);
 }

@@ -125,7 +125,9 @@ typedef enum { HC_MODE_FUSED = 0, HC_MODE_STEP = 1 } hc_mode_t;
 
 /*
  * Options; pass NULL for the defaults (fused, ranks_per_server 1, one loop,
- * no scratch).  struct_size must be sizeof(hc_opts_t).
+ * no scratch, device buffers).  struct_size must be sizeof(hc_opts_t), or
+ * offsetof(hc_opts_t, host_buffers) for callers built before that field
+ * (host_buffers is then 0).
  *  ranks_per_server : Pipeline and hierarchical only: ranks per server
  *                     (p_intra); P must be a multiple of it;
  *                     rank = server * p_intra + local.
@@ -140,6 +142,22 @@ typedef enum { HC_MODE_FUSED = 0, HC_MODE_STEP = 1 } hc_mode_t;
  *                     memory of at least hc_scratch_bytes() bytes, 16-byte
  *                     aligned, holding the ranks' intermediate partial sums.
  *                     Its contents on entry are ignored and on exit undefined.
+ *  host_buffers     : 0: send / recv are device memory (not checked).
+ *                     1: each send / recv buffer may also be page-locked host
+ *                     memory (cudaHostAlloc, cudaMallocHost or
+ *                     cudaHostRegister) whose device address equals its host
+ *                     address (unified addressing).  The kernels then read
+ *                     and write that memory directly over the host link
+ *                     (NVLink-C2C on Grace systems): no staging copies, and in
+ *                     fused mode every input byte crosses the link once
+ *                     towards the GPU and every output byte once back.  Each
+ *                     non-empty buffer is checked with
+ *                     cudaPointerGetAttributes: pageable (unregistered)
+ *                     memory, or host memory mapped at another device
+ *                     address, gives HC_ERR_INVALID_ARG and nothing is
+ *                     launched.  Step mode is allowed but moves its working
+ *                     traffic over the link as well.  The scratch stays
+ *                     device memory.
  */
 typedef struct {
     size_t struct_size;
@@ -148,6 +166,7 @@ typedef struct {
     size_t max_loop_bytes;
     void* scratch;
     size_t scratch_bytes;
+    int host_buffers;
 } hc_opts_t;
 
 /*

@@ -388,6 +388,31 @@ def test_rejects_bad_arguments_before_launch():
 
 
 @host_only
+def test_opts_host_buffers_field():
+    """hc_opts_t.host_buffers: only 0 or 1; a struct_size that ends before the
+    field (a caller built without it) is still accepted; with host_buffers = 1
+    every buffer is checked through the CUDA runtime, which without a GPU
+    reports HC_ERR_CUDA before anything is launched."""
+    P, n = 4, 1024
+    s, d = fake(P), fake(P, base=BASE + 64 * MB)
+    o = B.make_opts("fused")
+    o.struct_size = B.hc_opts_t.host_buffers.offset
+    assert status_of(B.hc_allreduce, s, d, P, n, "float32", "sum", "ring", o) == 5
+    o.struct_size = B.hc_opts_t.host_buffers.offset - 1
+    assert status_of(B.hc_allreduce, s, d, P, n, "float32", "sum", "ring", o) == 1
+    o = B.make_opts("fused")
+    o.host_buffers = 2
+    assert status_of(B.hc_allreduce, s, d, P, n, "float32", "sum", "ring", o) == 1
+    o = B.make_opts("fused", host_buffers=True)
+    assert status_of(B.hc_allreduce, s, d, P, n, "float32", "sum", "ring", o) == 5
+    # argument errors found before the pointer check keep their own status
+    bad = list(d)
+    bad[0] += 4
+    assert status_of(B.hc_allreduce, s, bad, P, n, "float32", "sum", "ring", o) == 3
+    assert status_of(B.hc_allreduce, s, d, 0, n, "float32", "sum", "ring", o) == 1
+
+
+@host_only
 def test_valid_call_without_gpu_reports_cuda_error():
     """Everything valid: the only failure left is the missing device."""
     P, n = 4, 1024
