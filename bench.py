@@ -101,9 +101,12 @@ def parse_args():
     ap.add_argument("--workload", default="ring_fp32_p8", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--sweep", choices=["small", "select"], default=None,
+    ap.add_argument("--sweep", choices=["small", "select", "hostlink", "hbm"], default=None,
                     help="small: RHD AllReduce latency sweep (P x n), eager vs graph mode; "
-                         "select: cost-model selector against measured times")
+                         "select: cost-model selector against measured times; "
+                         "hostlink: the default workload with pinned host buffers, zero-copy "
+                         "against staged copies; hbm: write-only and copy bandwidth of the "
+                         "device (torch kernels) beside the AllGather")
     return ap.parse_args()
 
 
@@ -117,13 +120,13 @@ def algorithmic_bytes(w):
     return (P + 1) * n * b  # allgather out of place
 
 
-def inputs_for(w, n=None):
+def inputs_for(w, n=None, seed=0):
     n = w["n"] if n is None else n
     if w["dtype"] == "float32":
-        return hc_inputs.gradients_f32(w["P"], n, seed=0, scale=w["scale"])
+        return hc_inputs.gradients_f32(w["P"], n, seed=seed, scale=w["scale"])
     if w["dtype"] == "bfloat16":
-        return hc_inputs.gradients_bf16(w["P"], n, seed=0, scale=w["scale"])
-    return hc_inputs.uniform_int32(w["P"], n, seed=0)
+        return hc_inputs.gradients_bf16(w["P"], n, seed=seed, scale=w["scale"])
+    return hc_inputs.uniform_int32(w["P"], n, seed=seed)
 
 
 def measured_peak():
@@ -457,21 +460,82 @@ def time_oracle_once(w, X):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(w, budget_s=10.0):
+# ---------------------------------------------------------------------------
+# the oracle on every host core: one spawned process per core, each replaying
+# the same schedule on its own seeded sample of the workload; two barriers
+# bracket every round, so a round's wall time covers all processes' replays
+# ---------------------------------------------------------------------------
+BARRIER_S = 600
+
+
+def _oracle_worker(w, ns, seed, rounds, start, end):
+    try:
+        X = inputs_for(w, ns, seed=seed)
+        time_oracle_once(w, X)  # load the library and page the inputs in
+        for _ in range(rounds):
+            start.wait(timeout=BARRIER_S)
+            time_oracle_once(w, X)
+            end.wait(timeout=BARRIER_S)
+    except Exception:
+        start.abort()
+        end.abort()
+        raise
+
+
+class ParallelOracle:
+    """`procs` spawned processes (spawn: safe after CUDA initialisation)."""
+
+    def __init__(self, w, ns, procs, rounds):
+        import multiprocessing as mp
+        ctx = mp.get_context("spawn")
+        self.start = ctx.Barrier(procs + 1)
+        self.end = ctx.Barrier(procs + 1)
+        self.procs = [ctx.Process(target=_oracle_worker, daemon=True,
+                                  args=(w, ns, 1000 + k, rounds, self.start, self.end))
+                      for k in range(procs)]
+        for p in self.procs:
+            p.start()
+
+    def round(self):
+        self.start.wait(timeout=BARRIER_S)
+        t0 = time.perf_counter()
+        self.end.wait(timeout=BARRIER_S)
+        return time.perf_counter() - t0
+
+    def close(self):
+        for p in self.procs:
+            p.join(timeout=60)
+
+
+def host_procs():
+    return max(1, os.cpu_count() or 1)
+
+
+def cpu_baseline(w, budget_s=5.0, parallel_s=8.0):
     ns = oracle_sample_n(w, 1 << 21)
     X = inputs_for(w, ns)
+    b = ESIZE[w["dtype"]]
     times = []
     t_start = time.perf_counter()
     while time.perf_counter() - t_start < budget_s or len(times) < 2:
         times.append(time_oracle_once(w, X))
         if len(times) >= 50:
             break
-    t = statistics.median(times)
-    return {"value": round(ns * ESIZE[w["dtype"]] / t / 1e9, 5), "unit": "GB/s", "cores": 1,
+    t1 = statistics.median(times)
+    procs = host_procs()
+    rounds = max(3, min(50, int(round(parallel_s / t1))))
+    po = ParallelOracle(w, ns, procs, rounds)
+    rt = [po.round() for _ in range(rounds)]
+    po.close()
+    tp = statistics.median(rt)
+    return {"value": round(procs * ns * b / tp / 1e9, 5), "unit": "GB/s", "cores": procs,
             "kind": "oracle",
-            "sample": "step-by-step replay of the same schedule on the first %d elements of each "
-                      "of the %d rank vectors, median of %d runs (%.1f s), single thread"
-                      % (ns, w["P"], len(times), sum(times)),
+            "sample": "step-by-step replay of the same schedule, one process per host core, each "
+                      "on its own seeded sample of %d elements of each of the %d rank vectors; "
+                      "median of %d rounds (%.1f s)" % (ns, w["P"], rounds, sum(rt)),
+            "single_thread": {"value": round(ns * b / t1 / 1e9, 5), "cores": 1,
+                              "sample": "the first %d elements of each rank vector, median of "
+                                        "%d runs (%.1f s)" % (ns, len(times), sum(times))},
             "cpu": cpu_model()}
 
 
@@ -492,17 +556,17 @@ def run_reference(args, w):
     if rank != 0:
         return
     ns = oracle_sample_n(w, 1 << 20)
-    X = inputs_for(w, ns)
+    procs = host_procs()
+    po = ParallelOracle(w, ns, procs, args.warmup + args.steps)
     for _ in range(args.warmup):
-        time_oracle_once(w, X)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        time_oracle_once(w, X)
-    total = time.perf_counter() - t0
+        po.round()
+    total = sum(po.round() for _ in range(args.steps))
+    po.close()
     ms = total / args.steps * 1e3
-    value = ns * ESIZE[w["dtype"]] / (ms * 1e-3) / 1e9
-    sample = ("oracle step-by-step replay (plain C, one thread) of the same schedule on the "
-              "first %d elements of each of the %d rank vectors per step" % (ns, w["P"]))
+    value = procs * ns * ESIZE[w["dtype"]] / (ms * 1e-3) / 1e9
+    sample = ("oracle step-by-step replay (plain C) of the same schedule, one process per host "
+              "core (%d), each on its own seeded sample of %d elements of each of the %d rank "
+              "vectors per step" % (procs, ns, w["P"]))
     line = {
         "impl": "reference",
         "metric": METRIC,
@@ -520,8 +584,8 @@ def run_reference(args, w):
         "config": {"workload": w["desc"], "algo": w["algo"], "collective": w["coll"],
                    "P": w["P"], "elements_per_rank": w["n"], "mode": "oracle",
                    "sample_elements_per_rank": ns},
-        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                         "sample": sample, "cpu": cpu_model()},
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": procs,
+                         "kind": "oracle", "sample": sample, "cpu": cpu_model()},
         "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -652,6 +716,133 @@ def sweep_select(args):
         print(json.dumps(line), flush=True)
 
 
+def sweep_hostlink(args):
+    """The default workload (Ring AllReduce fp32 sum, P=8, 16,777,216
+    elements per rank) with its inputs and outputs in pinned host memory:
+    the copy engines alone and overlapped, the staged call (copy in, fused
+    kernel, copy out) and the fused kernel on the host buffers
+    (host_buffers=1), each checked bit for bit against the device path."""
+    import torch
+    from collective_communication_algorithms_gb300 import _binding as B
+    w = WORKLOADS["ring_fp32_p8"]
+    P, n, b = w["P"], w["n"], 4
+    torch.cuda.set_device(0)
+    B.lib()
+    s0 = torch.cuda.current_stream()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    Xh = torch.from_numpy(inputs_for(w)).pin_memory()
+    Yh = torch.empty_like(Xh).pin_memory()
+    Xd = Xh.to("cuda")
+    Yd = torch.empty_like(Xd)
+    Zd = torch.empty_like(Xd)
+    dev_opts = B.make_opts("fused")
+    host_opts = B.make_opts("fused", host_buffers=True)
+
+    def ar(x, y, opts):
+        B.hc_allreduce([x[r].data_ptr() for r in range(P)], [y[r].data_ptr() for r in range(P)],
+                       P, n, "float32", "sum", "ring", opts, s0.cuda_stream)
+
+    def both_directions():
+        ev = torch.cuda.Event()
+        ev.record(s0)
+        s1.wait_event(ev)
+        s2.wait_event(ev)
+        with torch.cuda.stream(s1):
+            Zd.copy_(Xh, non_blocking=True)
+        with torch.cuda.stream(s2):
+            Yh.copy_(Yd, non_blocking=True)
+        for s in (s1, s2):
+            e = torch.cuda.Event()
+            e.record(s)
+            s0.wait_event(e)
+
+    def staged():
+        Xd.copy_(Xh, non_blocking=True)
+        ar(Xd, Yd, dev_opts)
+        Yh.copy_(Yd, non_blocking=True)
+
+    ar(Xd, Yd, dev_opts)
+    torch.cuda.synchronize()
+    ref = Yd.cpu()
+    cases = [("h2d copy, 512 MiB", lambda: Xd.copy_(Xh, non_blocking=True), None),
+             ("d2h copy, 512 MiB", lambda: Yh.copy_(Yd, non_blocking=True), None),
+             ("h2d and d2h copies on two streams", both_directions, None),
+             ("staged: h2d copy, fused kernel, d2h copy", staged, lambda: Yh),
+             ("fused kernel, device buffers", lambda: ar(Xd, Yd, dev_opts), lambda: Yd.cpu()),
+             ("fused kernel, host inputs, device outputs", lambda: ar(Xh, Yd, host_opts),
+              lambda: Yd.cpu()),
+             ("fused kernel, device inputs, host outputs", lambda: ar(Xd, Yh, host_opts),
+              lambda: Yh),
+             ("fused kernel, host inputs and outputs", lambda: ar(Xh, Yh, host_opts),
+              lambda: Yh)]
+    for name, fn, out in cases:
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s0)
+        for _ in range(args.steps):
+            fn()
+        e1.record(s0)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        line = {"sweep": "hostlink", "case": name, "ms": round(ms, 4),
+                "algbw_GBps": round(n * b / ms / 1e6, 2)}
+        if out is not None:
+            line["bit_exact"] = bool(torch.equal(out(), ref))
+            Yh.zero_()
+            Yd.zero_()
+        print(json.dumps(line), flush=True)
+
+
+def sweep_hbm(args):
+    """Device-memory ceilings for write-heavy collectives: torch's fill
+    (write only), copy (read = write) and broadcast copy (one read, P = 8
+    writes, the AllGather's mix) over 1 GiB, and the fused Ring AllGather
+    fp32 P=8 (writes P bytes per byte read), in GB/s of bytes moved."""
+    import torch
+    from collective_communication_algorithms_gb300 import _binding as B
+    torch.cuda.set_device(0)
+    B.lib()
+    s0 = torch.cuda.current_stream()
+    nb = 1 << 30
+    a = torch.empty(nb // 4, dtype=torch.float32, device="cuda")
+    c = torch.empty_like(a)
+    a.normal_()
+    w = WORKLOADS["ring_fp32_p8_ag"]
+    P, n = w["P"], w["n"]
+    segs = [B.hc_segment_range("ring", "allgather", P, n, "float32", k) for k in range(P)]
+    X = torch.from_numpy(inputs_for(w)).cuda()
+    ag_in = [X[k, off:off + ln].clone() for k, (off, ln) in enumerate(segs)]
+    Y = torch.empty_like(X)
+    opts = B.make_opts("fused")
+    src = a[:nb // 4 // P]
+    dst = c.view(P, nb // 4 // P)
+    cases = [("fill (write only), 1 GiB", lambda: c.fill_(1.0), nb),
+             ("copy (read 1 GiB, write 1 GiB)", lambda: c.copy_(a), 2 * nb),
+             ("broadcast copy (read 128 MiB, write 8 x 128 MiB)",
+              lambda: dst.copy_(src.expand(P, -1)), nb + nb // P),
+             ("fused Ring AllGather fp32 P=8 (read n b, write P n b)",
+              lambda: B.hc_allgather([t.data_ptr() for t in ag_in], [Y[r].data_ptr() for r in range(P)],
+                                     P, n, "float32", "ring", opts, s0.cuda_stream),
+              (P + 1) * n * 4)]
+    for name, fn, moved in cases:
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(s0)
+        for _ in range(args.steps):
+            fn()
+        e1.record(s0)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        print(json.dumps({"sweep": "hbm", "case": name, "ms": round(ms, 4),
+                          "GBps_moved": round(moved / ms / 1e6, 1)}), flush=True)
+
+
 def main():
     args = parse_args()
     if args.sweep == "small":
@@ -659,6 +850,12 @@ def main():
         return
     if args.sweep == "select":
         sweep_select(args)
+        return
+    if args.sweep == "hostlink":
+        sweep_hostlink(args)
+        return
+    if args.sweep == "hbm":
+        sweep_hbm(args)
         return
     if args.warmup < 3:
         args.warmup = 3

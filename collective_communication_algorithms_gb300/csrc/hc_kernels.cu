@@ -138,8 +138,11 @@ fused_allgather(const __grid_constant__ FusedParams p) {
 // AllReduce / ReduceScatter shape tried: with 8 warps per SM the barrier
 // waits and the reduction could not hide behind the copies.)
 // ---------------------------------------------------------------------------
-constexpr int kAgTile = 8192;           // bytes per stage
-constexpr int kAgStages = 8;
+// 32 KB tiles, 6 stages: 192 KB of shared memory, one block per SM.  Against
+// 8 KB x 8 (three blocks per SM) this measured 2-3 % faster for P = 8 and 14 %
+// faster for P = 32 (AllGather fp32, GB300), where each tile feeds 32 stores.
+constexpr int kAgTile = 32768;          // bytes per stage
+constexpr int kAgStages = 6;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ int hc_device_error;
@@ -198,7 +201,7 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 }
 
 // AllGather, TMA-staged: one thread streams the owner's segment through
-// shared memory in 8 KB tiles, each tile loaded once and bulk-stored to every
+// shared memory in 32 KB tiles, each tile loaded once and bulk-stored to every
 // rank (the owner's own copy only when it is not already in place).
 // Broadcast: one segment owned by the root.
 template <int ES>

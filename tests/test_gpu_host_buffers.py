@@ -119,9 +119,10 @@ def check_host(coll, algo, X, dtype, op, mode, p_intra=1, root=0, recv_on_device
         assert same_bits(res[r], want[r], dtype), (coll, algo, dtype, op, mode, P, n, r)
 
 
-# 300,007 fp32 elements over 8 ranks puts 150 KB in each segment: device
-# buffers of that size take the TMA AllGather path, host buffers must not
-SIZES = (37, 4099, 300007)
+# 1,100,007 elements of a 4-byte type over 8 ranks put 537 KB in each
+# segment: device buffers of that size take the TMA AllGather path (at least
+# 16 tiles of 32 KB), host buffers must not
+SIZES = (37, 4099, 1100007)
 
 
 @pytest.mark.parametrize("mode", ["fused", "step"])
@@ -143,14 +144,14 @@ def test_host_buffers_allreduce_ops_hier_and_broadcast(mode):
         check_host("allreduce", "rhd", X, "float32", op, mode)
     X = hc_inputs.rank_buffers("bfloat16", 32, 65548, seed=4)
     check_host("allreduce", "hier", X, "bfloat16", "sum", mode, p_intra=8)
-    X = hc_inputs.rank_buffers("float32", 6, 300007, seed=5)
+    X = hc_inputs.rank_buffers("float32", 6, 1100007, seed=5)
     for root in (0, 3):
         check_host("broadcast", "rhd", X, "float32", "sum", mode, root=root)
 
 
 def test_host_inputs_device_outputs():
     """Mixed placement: inputs in pinned host memory, outputs in device memory."""
-    X = hc_inputs.rank_buffers("float32", 8, 300007, seed=6)
+    X = hc_inputs.rank_buffers("float32", 8, 1100007, seed=6)
     check_host("allreduce", "ring", X, "float32", "sum", "fused", recv_on_device=True)
     check_host("allgather", "ring", X, "float32", "sum", "fused", recv_on_device=True)
 

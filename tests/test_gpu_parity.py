@@ -175,11 +175,11 @@ def test_uses_the_given_stream():
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_tma_staged_paths(algo, dtype):
     """Segments long enough for the TMA-staged AllGather (at least 16 tiles of
-    8 KB per segment), with a partial last tile and a ragged end; AllReduce and
+    32 KB per segment), with a partial last tile and a ragged end; AllReduce and
     ReduceScatter at the same sizes (register path with every launch shape the
     library picks: 4- and 2-byte types, sum and max)."""
     from collective_communication_algorithms_gb300 import _binding as B
-    per_seg = 40000 if dtype != "bfloat16" else 70000
+    per_seg = 70000 if dtype != "bfloat16" else 135000
     for P in (2, 3, 5, 8):
         pin = intra_for(algo, P) if algo != "pipeline" else (2 if P % 2 == 0 else 1)
         n = P * per_seg + 13
@@ -200,7 +200,8 @@ def test_broadcast(mode, dtype):
     """RHD Broadcast: every rank ends with the root's vector, bit for bit."""
     for P in (1, 2, 3, 5, 8, 12, 16):
         roots = range(P) if P <= 8 else (0, 1, P // 2, P - 1)
-        for n in (1, 37, 4099, 80000 + 3):
+        # 300,007 elements: the TMA-staged path (at least 16 tiles of 32 KB)
+        for n in (1, 37, 4099, 80000 + 3, 300007):
             X = inputs(dtype, P, n, seed=P * 13 + n, op="sum")
             for root in roots:
                 for in_place in (False, True):
