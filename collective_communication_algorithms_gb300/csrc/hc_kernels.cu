@@ -34,9 +34,13 @@ namespace {
 // step kernel
 // ---------------------------------------------------------------------------
 constexpr int kStepThreads = 256;
+constexpr int kStepBatch = 8;  // input loads in flight per vector
 
-template <hc_dtype_t DT, hc_op_t OP, int MAXI>
-__global__ void __launch_bounds__(kStepThreads)
+// BATCH: input loads issued before reducing (1 for launches whose items
+// have at most two inputs, where 8 blocks per SM give the loads in flight;
+// kStepBatch for wider items, e.g. the Pipeline's intra-server mesh reduce)
+template <hc_dtype_t DT, hc_op_t OP, int MAXI, int BATCH>
+__global__ void __launch_bounds__(kStepThreads, BATCH == 1 ? 8 : 4)
 step_kernel(const __grid_constant__ StepParams<MAXI> p) {
     constexpr int ES = DT_<DT>::ES;
     constexpr int A = DT_<DT>::A;
@@ -48,6 +52,12 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
     const int64_t nthreads = (int64_t)(cend - I.cta_begin) * blockDim.x;
     const int64_t t0 = (int64_t)(b - I.cta_begin) * blockDim.x + threadIdx.x;
     const int nseg = I.seg_width * I.seg_reps;
+    // Programmatic dependent launch: this grid may be scheduled while the
+    // previous step's grid drains.  Wait for that grid to complete (and its
+    // writes to be visible) before touching any buffer, then let the next
+    // step's grid be scheduled.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     for (int si = 0; si < nseg; si++) {
         const int seg = I.seg_first + (si / I.seg_width) * I.seg_stride + (si % I.seg_width);
@@ -59,14 +69,28 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
         const int64_t lo = sbeg + p.lo;
         for (int64_t e = lo + t0 * A; e < hi; e += nthreads * A) {
             const uintptr_t off = (uintptr_t)e * ES;
-            int r = I.in_rot;
             if (e + A <= hi) {
-                uint4 v = ld_vec(p.base[I.in_loc][I.in_base + r] + off);
-                for (int j = 1; j < I.in_cnt; j++) {
-                    if (++r == I.in_mod) r = 0;
-                    v = vop<DT, OP>(v, ld_vec(p.base[I.in_loc][I.in_base + r] + off));
+                // issue the accumulator's and up to BATCH inputs' loads
+                // before reducing them in the item's order
+                uint4 acc = make_uint4(0, 0, 0, 0);
+                if (I.acc_rank >= 0) acc = ld_vec(p.base[I.acc_loc][I.acc_rank] + off);
+                uint4 v = acc;
+                int r = I.in_rot;
+                for (int c = 0; c < I.in_cnt; c += BATCH) {
+                    const int m = I.in_cnt - c < BATCH ? I.in_cnt - c : BATCH;
+                    uint4 x[BATCH];
+#pragma unroll
+                    for (int q = 0; q < BATCH; q++) {
+                        if (q < m) {
+                            x[q] = ld_vec(p.base[I.in_loc][I.in_base + r] + off);
+                            if (++r == I.in_mod) r = 0;
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < BATCH; q++)
+                        if (q < m) v = (c == 0 && q == 0) ? x[0] : vop<DT, OP>(v, x[q]);
                 }
-                if (I.acc_rank >= 0) v = vop<DT, OP>(ld_vec(p.base[I.acc_loc][I.acc_rank] + off), v);
+                if (I.acc_rank >= 0) v = vop<DT, OP>(acc, v);
                 int o = I.out_rot;
                 for (int j = 0; j < I.out_cnt; j++) {
                     st_vec(p.base[I.out_loc][I.out_base + o] + off, v);
@@ -300,22 +324,39 @@ bool allow_smem(void* fn, int bytes) {
     return true;
 }
 
-template <int MAXI, hc_dtype_t DT>
+template <int MAXI, int BATCH, hc_dtype_t DT>
 void* pick_step_op(hc_op_t op) {
     switch (op) {
-    case HC_SUM: return (void*)step_kernel<DT, HC_SUM, MAXI>;
-    case HC_PROD: return (void*)step_kernel<DT, HC_PROD, MAXI>;
-    case HC_MAX: return (void*)step_kernel<DT, HC_MAX, MAXI>;
-    default: return (void*)step_kernel<DT, HC_MIN, MAXI>;
+    case HC_SUM: return (void*)step_kernel<DT, HC_SUM, MAXI, BATCH>;
+    case HC_PROD: return (void*)step_kernel<DT, HC_PROD, MAXI, BATCH>;
+    case HC_MAX: return (void*)step_kernel<DT, HC_MAX, MAXI, BATCH>;
+    default: return (void*)step_kernel<DT, HC_MIN, MAXI, BATCH>;
     }
 }
-template <int MAXI>
+template <int MAXI, int BATCH>
 void* pick_step(hc_dtype_t dt, hc_op_t op) {
     switch (dt) {
-    case HC_INT32: return pick_step_op<MAXI, HC_INT32>(op);
-    case HC_FLOAT32: return pick_step_op<MAXI, HC_FLOAT32>(op);
-    default: return pick_step_op<MAXI, HC_BFLOAT16>(op);
+    case HC_INT32: return pick_step_op<MAXI, BATCH, HC_INT32>(op);
+    case HC_FLOAT32: return pick_step_op<MAXI, BATCH, HC_FLOAT32>(op);
+    default: return pick_step_op<MAXI, BATCH, HC_BFLOAT16>(op);
     }
+}
+
+// Blocks of a step kernel resident per SM (cached per kernel).
+int resident_blocks(void* fn) {
+    static void* fns[256];
+    static int val[256];
+    static int nfns = 0;
+    for (int i = 0; i < nfns; i++)
+        if (fns[i] == fn) return val[i];
+    int v = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fn, kStepThreads, 0) != cudaSuccess || v < 1)
+        v = 1;
+    if (nfns < 256) {
+        fns[nfns] = fn;
+        val[nfns++] = v;
+    }
+    return v;
 }
 
 constexpr int kSmallItems = 48;   // parameter block under 4 KB
@@ -325,7 +366,7 @@ template <int MAXI>
 cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t first, size_t count,
                               hc_dtype_t dt, hc_op_t op,
                               const uintptr_t (&base)[LOC_COUNT][kMaxRanks],
-                              cudaStream_t stream, int max_ctas) {
+                              cudaStream_t stream, int sm_count) {
     static thread_local StepParams<MAXI> p;  // large: keep it off the stack
     std::memcpy(p.base, base, sizeof(p.base));
     p.L = plan.lay.L;
@@ -337,13 +378,30 @@ cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t firs
     part.lo = L.lo;
     part.hi = L.hi;
     part.items.assign(L.items.begin() + first, L.items.begin() + first + count);
-    const int grid = assign_ctas(part, plan.lay, kStepThreads, max_ctas);
+    int widest = 1;
+    for (const DevItem& it : part.items) widest = std::max(widest, (int)it.in_cnt);
+    void* fn = widest >= 3 ? pick_step<MAXI, kStepBatch>(dt, op) : pick_step<MAXI, 1>(dt, op);
+    // one wave of resident blocks
+    const int grid = assign_ctas(part, plan.lay, kStepThreads, sm_count * resident_blocks(fn));
     p.nitems = (int)count;
     p.total_ctas = grid;
     std::memcpy(p.items, part.items.data(), count * sizeof(DevItem));
-    void* fn = pick_step<MAXI>(dt, op);
     void* args[] = {&p};
-    return cudaLaunchKernel(fn, dim3(grid), dim3(kStepThreads), args, 0, stream);
+    // programmatic stream serialization: the kernel waits for its
+    // predecessor itself (griddepcontrol.wait), so its launch and block
+    // scheduling overlap the previous step's tail
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kStepThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace
@@ -352,17 +410,16 @@ cudaError_t launch_step(const Plan& plan, int P, hc_dtype_t dt, hc_op_t op,
                         const uintptr_t (&base)[LOC_COUNT][kMaxRanks], cudaStream_t stream,
                         int sm_count) {
     (void)P;
-    const int max_ctas = sm_count * (2048 / kStepThreads);
     for (const PlanLaunch& L : plan.launches) {
         size_t ni = L.items.size();
         cudaError_t e = cudaSuccess;
         if (ni <= (size_t)kSmallItems) {
-            e = launch_step_items<kSmallItems>(plan, L, 0, ni, dt, op, base, stream, max_ctas);
+            e = launch_step_items<kSmallItems>(plan, L, 0, ni, dt, op, base, stream, sm_count);
         } else {
             // items of one step are independent, so a step may be split
             for (size_t f = 0; f < ni && e == cudaSuccess; f += kLargeItems)
                 e = launch_step_items<kLargeItems>(plan, L, f, std::min(ni - f, (size_t)kLargeItems),
-                                                   dt, op, base, stream, max_ctas);
+                                                   dt, op, base, stream, sm_count);
         }
         if (e != cudaSuccess) return e;
     }
