@@ -318,6 +318,11 @@ fused_reduce(const __grid_constant__ FusedParams p) {
     const int64_t send_ = (sbeg + p.L < p.n) ? sbeg + p.L : p.n;
     const int64_t nfull = (send_ - sbeg) / A;
     const int64_t chunk = (int64_t)V * blockDim.x;
+    // programmatic dependent launch: wait for the previous grid on the
+    // stream (and its writes) before touching a buffer, then let the next
+    // grid be scheduled
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int64_t base = (int64_t)blockIdx.x * chunk; base < nfull; base += (int64_t)gridDim.x * chunk) {
         auto load = [&](int r) -> VecN<V> {
             VecN<V> x;

@@ -134,6 +134,8 @@ fused_allgather(const __grid_constant__ FusedParams p) {
     const int64_t nfull = (send_ - sbeg) / A;
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const bool skip_own = (p.skip_mask >> k) & 1ull;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nfull; v += stride) {
         const uintptr_t off = (uintptr_t)(sbeg + v * A) * ES;
         const uint4 x = ld_stream(p.src[k] + off);
@@ -239,6 +241,8 @@ fused_allgather_tma(const __grid_constant__ FusedParams p) {
     const int64_t send_ = sbeg + p.L < p.n ? sbeg + p.L : p.n;
     const int64_t nfull = send_ > sbeg ? (send_ - sbeg) / A : 0;
     const bool skip_own = (p.skip_mask >> k) & 1ull;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (threadIdx.x == 0) {
         uint64_t* full = (uint64_t*)(smem + (size_t)kAgStages * kAgTile);
         const int64_t nbytes = nfull * 16;
@@ -306,6 +310,25 @@ void* pick_reduce(hc_algo_t algo, int coll, hc_dtype_t dt, hc_op_t op, int V, in
     case HC_ALGO_HIER: return pick_fused_hier(coll, dt, op, V);
     default: return pick_fused_pipe(coll, dt, op, V);
     }
+}
+
+// Launch with programmatic stream serialization: the kernel waits for the
+// previous grid on the stream itself (griddepcontrol.wait), so its launch
+// and block scheduling overlap that grid's tail.
+cudaError_t launch_pdl(void* fn, dim3 grid, dim3 block, void** args, size_t smem,
+                       cudaStream_t stream) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 // Raise a kernel's dynamic shared memory limit to at least `bytes` (the
@@ -387,21 +410,7 @@ cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t firs
     p.total_ctas = grid;
     std::memcpy(p.items, part.items.data(), count * sizeof(DevItem));
     void* args[] = {&p};
-    // programmatic stream serialization: the kernel waits for its
-    // predecessor itself (griddepcontrol.wait), so its launch and block
-    // scheduling overlap the previous step's tail
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kStepThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelExC(&cfg, fn, args);
+    return launch_pdl(fn, dim3(grid), dim3(kStepThreads), args, 0, stream);
 }
 
 }  // namespace
@@ -481,13 +490,13 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
             const int64_t tiles = (seg_bytes + kAgTile - 1) / kAgTile;
             const int gx = (int)std::max<int64_t>(
                 1, std::min<int64_t>(tiles, (int64_t)sm_count * std::max(1, per_sm) / S));
-            return cudaLaunchKernel(fn, dim3(gx, S), dim3(32), args, smem, stream);
+            return launch_pdl(fn, dim3(gx, S), dim3(32), args, smem, stream);
         }
         void* fn = es == 2 ? (void*)fused_allgather<2> : (void*)fused_allgather<4>;
         const int64_t vecs = (lay.L + lay.A - 1) / lay.A;
         const int64_t want = std::max<int64_t>(1, (vecs + kFusedThreads - 1) / kFusedThreads);
         const int gx = (int)std::min(want, std::max<int64_t>(1, (int64_t)sm_count * 4 / S));
-        return cudaLaunchKernel(fn, dim3(gx, S), dim3(kFusedThreads), args, 0, stream);
+        return launch_pdl(fn, dim3(gx, S), dim3(kFusedThreads), args, 0, stream);
     }
 
     const int COLL = a.coll == HC_COLL_ALLREDUCE ? 0 : 1;
@@ -531,7 +540,7 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     const int64_t vecs = (lay.L + lay.A - 1) / lay.A;
     const int64_t want = std::max<int64_t>(1, (vecs + (int64_t)V * kFusedThreads - 1) / ((int64_t)V * kFusedThreads));
     const int gx = (int)std::min(want, std::max<int64_t>(1, (int64_t)sm_count * per_sm / S));
-    return cudaLaunchKernel(fn, dim3(gx, S), dim3(kFusedThreads), args, 0, stream);
+    return launch_pdl(fn, dim3(gx, S), dim3(kFusedThreads), args, 0, stream);
 }
 
 cudaError_t read_device_error(bool clear, int* status) {
