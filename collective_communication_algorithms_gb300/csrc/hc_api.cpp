@@ -529,10 +529,12 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
                            hc_dtype_t dtype, hc_mode_t mode, hc_algo_t* out_algo,
                            double* predicted_us) {
     // measured on GB300 (bench.py workloads and the small-message sweep):
-    // host cost of one eager launch, device time between dependent kernels,
-    // HBM bandwidth and the fraction of it step / fused kernels reach
-    const double kHostLaunchUs = 4.6, kDeviceStepUs = 2.5;
-    const double kBandwidth = 6800e9, kStepFrac = 0.86, kFusedFrac = 0.93;
+    // host cost of a call and of each of its launches, device time per
+    // dependent launch, HBM bandwidth and the fraction of it step / fused
+    // kernels reach (measured on GB300, kernels launched with programmatic
+    // stream serialization)
+    const double kHostCallUs = 3.5, kHostLaunchUs = 2.3, kDeviceStepUs = 3.0;
+    const double kBandwidth = 6800e9, kStepFrac = 0.83, kFusedFrac = 0.93;
     if (!out_algo || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
     if (mode != HC_MODE_FUSED && mode != HC_MODE_STEP) return HC_ERR_INVALID_ARG;
     if (P < 1 || P > kMaxRanks) return HC_ERR_INVALID_ARG;
@@ -554,7 +556,7 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
         const int launches = mode == HC_MODE_STEP ? st.launches_step : st.launches_fused;
         const double bytes = mode == HC_MODE_STEP ? (double)st.step_bytes : (double)st.fused_bytes;
         const double frac = mode == HC_MODE_STEP ? kStepFrac : kFusedFrac;
-        const double host = launches * kHostLaunchUs;
+        const double host = kHostCallUs + launches * kHostLaunchUs;
         const double device = launches * kDeviceStepUs + bytes / (frac * kBandwidth) * 1e6;
         const double t = host > device ? host : device;
         if (!have || t < best) {

@@ -377,11 +377,12 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
  * bytes its kernels move over the HBM bandwidth (beta; the reduction, gamma,
  * hides under the memory traffic).  Launches are queued asynchronously, so
  * the host's launch cost and the device time overlap:
- *   t = max(launches * alpha_host, launches * alpha_dev + bytes / (f * B))
+ *   t = max(c_host + launches * alpha_host,
+ *           launches * alpha_dev + bytes / (f * B))
  * with launches and bytes (step or fused mode) from hc_schedule_stats and
- * alpha_host = 4.6 us per eager launch, alpha_dev = 2.5 us between dependent
- * kernels, f = 0.86 (step) / 0.93 (fused), B = 6800 GB/s, all measured on
- * GB300.  Candidates: Ring and RHD;
+ * c_host = 3.5 us per call, alpha_host = 2.3 us per launch, alpha_dev =
+ * 3.0 us per dependent launch, f = 0.83 (step) / 0.93 (fused), B = 6800 GB/s,
+ * all measured on GB300.  Candidates: Ring and RHD;
  * Pipeline and, for an AllReduce, the hierarchical AllReduce when
  * ranks_per_server > 1 divides P.  On a tie the earlier candidate wins (Ring,
  * RHD, Pipeline, hierarchical).

@@ -554,16 +554,16 @@ def test_hier_is_allreduce_only():
 
 
 def test_cost_model_selector():
-    """hc_select_algo: the cheapest schedule under t = max(launches * alpha_host,
-    launches * alpha_dev + bytes / (f B)), recomputed here from
+    """hc_select_algo: the cheapest schedule under t = max(c_host + launches *
+    alpha_host, launches * alpha_dev + bytes / (f B)), recomputed here from
     hc_schedule_stats; small messages pick the schedule with the fewest
     launches; the hierarchical schedule is offered only with servers."""
     def model(algo, coll, P, n, mode, rps):
         st, _ = B.hc_schedule_stats(algo, coll, P, n, "float32", rps, 0)
         L = st["launches_step"] if mode == "step" else st["launches_fused"]
         by = st["step_bytes"] if mode == "step" else st["fused_bytes"]
-        f = 0.86 if mode == "step" else 0.93
-        return max(L * 4.6, L * 2.5 + by / (f * 6800e9) * 1e6)
+        f = 0.83 if mode == "step" else 0.93
+        return max(3.5 + L * 2.3, L * 3.0 + by / (f * 6800e9) * 1e6)
     for coll in ("allreduce", "reducescatter", "allgather"):
         for P, rps in ((2, 1), (5, 1), (8, 1), (12, 4), (16, 4), (32, 8), (64, 8)):
             for n in (256, 4096, 1 << 20, 16 << 20):
