@@ -171,6 +171,43 @@ def test_uses_the_given_stream():
     assert same_bits(res[0], Y[0], "float32")
 
 
+def _special_values(dtype, P, n, seed):
+    """Bit patterns max/min must order by IEEE totalOrder: +-0, +-Inf, NaNs of
+    both signs with several payloads, subnormals, the extremes, and random
+    values, scattered over the ranks."""
+    rng = np.random.default_rng(seed)
+    if dtype == "bfloat16":
+        pool = np.array([0x0000, 0x8000, 0x7F80, 0xFF80, 0x7FC0, 0xFFC0, 0x7F81, 0xFF81,
+                         0x7FFF, 0xFFFF, 0x0001, 0x8001, 0x007F, 0x807F, 0x7F7F, 0xFF7F,
+                         0x3F80, 0xBF80], dtype=np.uint16)
+        X = rng.integers(0, 1 << 16, (P, n), dtype=np.uint32).astype(np.uint16)
+    else:
+        pool = np.array([0x00000000, 0x80000000, 0x7F800000, 0xFF800000, 0x7FC00000, 0xFFC00000,
+                         0x7F800001, 0xFF800001, 0x7FFFFFFF, 0xFFFFFFFF, 0x00000001, 0x80000001,
+                         0x007FFFFF, 0x807FFFFF, 0x7F7FFFFF, 0xFF7FFFFF, 0x3F800000, 0xBF800000],
+                        dtype=np.uint32)
+        X = rng.integers(0, 1 << 32, (P, n), dtype=np.uint64).astype(np.uint32)
+    pick = rng.random((P, n)) < 0.5
+    X[pick] = pool[rng.integers(0, pool.size, int(pick.sum()))]
+    return X if dtype == "bfloat16" else X.view(np.float32)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("dtype", ["float32", "bfloat16"])
+@pytest.mark.parametrize("op", ["max", "min"])
+def test_max_min_special_values(algo, dtype, op):
+    """max / min of +-0, +-Inf, NaN payloads, subnormals and random bit
+    patterns follow IEEE totalOrder bit for bit (oracle replay), fused and
+    step mode, AllReduce and ReduceScatter."""
+    for P in (3, 8, 12):
+        pin = intra_for(algo, P)
+        for n in (4099, 65548):
+            X = _special_values(dtype, P, n, seed=P * 7 + n)
+            for mode in ("fused", "step"):
+                check("allreduce", algo, X, dtype, op, mode, False, pin)
+                check("reducescatter", algo, X, dtype, op, mode, False, pin)
+
+
 def test_concurrent_step_mode_calls_on_many_streams():
     """Small step-mode collectives (one programmatically dependent launch per
     step) issued on 6 streams at once, 40 calls each, every call on its own
