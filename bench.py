@@ -288,6 +288,11 @@ def run_ours(args, w):
     ev1 = torch.cuda.Event(enable_timing=True)
     ka = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    # a spin kernel ahead of the timed region lets the host enqueue all K
+    # steps before the device starts them, so the events time the device
+    # work and not the host's launch rate (one call from Python takes tens of
+    # microseconds, about as long as a 0.1 ms collective)
+    torch.cuda._sleep(int(4e5 * max(args.steps, 10)))  # ~0.2 ms per step at 2 GHz
     ev0.record(stream)
     for i in range(args.steps):
         ka[i].record(stream)
