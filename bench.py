@@ -147,6 +147,16 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def hold_device(steps):
+    """Queue a spin kernel on the current stream ahead of a timed region, so
+    that the host enqueues all `steps` calls before the device starts them
+    and the events time the device work, not the host's launch rate (one
+    call from Python takes tens of microseconds, about as long as a 0.1 ms
+    collective).  About 0.2 ms per step at 2 GHz."""
+    import torch
+    torch.cuda._sleep(int(4e5 * max(steps, 10)))
+
+
 def traffic_from_profiles(workload):
     """dram read+write bytes per launch of the dominant kernel from a
     committed ncu summary, if it was taken on the current kernel source."""
@@ -213,6 +223,28 @@ class ClockSampler:
             return {"error": "no samples"}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
                 "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# replicas: one process per GPU, each running the whole collective on its own
+# buffers (no data-path exchange); the job's time is the slowest rank's
+# ---------------------------------------------------------------------------
+def max_over_ranks(values, world, device):
+    """Element-wise maximum of a list of floats over all ranks of the
+    default process group (the values themselves when world == 1)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def replica_algbw(world, bytes_per_rank, ms):
+    """Whole-job algbw in GB/s: every replica moves bytes_per_rank of
+    per-rank data in ms (the slowest rank's time)."""
+    return world * bytes_per_rank / (ms * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -288,11 +320,7 @@ def run_ours(args, w):
     ev1 = torch.cuda.Event(enable_timing=True)
     ka = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    # a spin kernel ahead of the timed region lets the host enqueue all K
-    # steps before the device starts them, so the events time the device
-    # work and not the host's launch rate (one call from Python takes tens of
-    # microseconds, about as long as a 0.1 ms collective)
-    torch.cuda._sleep(int(4e5 * max(args.steps, 10)))  # ~0.2 ms per step at 2 GHz
+    hold_device(args.steps)
     ev0.record(stream)
     for i in range(args.steps):
         ka[i].record(stream)
@@ -305,14 +333,9 @@ def run_ours(args, w):
     clocks = sampler.stop()
     total_ms = ev0.elapsed_time(ev1)
     kern_ms = [a.elapsed_time(bb) for a, bb in zip(ka, kb)]
-    if world > 1:
-        t = torch.tensor([total_ms, statistics.mean(kern_ms)], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, kern_avg = float(t[0]), float(t[1])
-    else:
-        kern_avg = statistics.mean(kern_ms)
+    total_ms, kern_avg = max_over_ranks([total_ms, statistics.mean(kern_ms)], world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * n * b / (ms_per_step * 1e-3) / 1e9
+    value = replica_algbw(world, n * b, ms_per_step)
 
     # end to end through the C ABI with host buffers (pinned), copies timed
     e2e = None
@@ -391,11 +414,8 @@ def run_ours(args, w):
             same = torch.equal(Yh, recv.cpu())
         if not same:
             raise SystemExit("e2e outputs differ from the device-buffer outputs")
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev, dtype=torch.float64)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t[0])
-        e2e = {"value": round(world * n * b / (e_ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+        e_ms = max_over_ranks([e_ms], world, dev)[0]
+        e2e = {"value": round(replica_algbw(world, n * b, e_ms), 3), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": round(e_ms, 4), "path": e2e_path}
 
@@ -804,8 +824,10 @@ def sweep_hostlink(args):
 def sweep_hbm(args):
     """Device-memory ceilings for write-heavy collectives: torch's fill
     (write only), copy (read = write) and broadcast copy (one read, P = 8
-    writes, the AllGather's mix) over 1 GiB, and the fused Ring AllGather
-    fp32 P=8 (writes P bytes per byte read), in GB/s of bytes moved."""
+    writes, the AllGather's mix) over 1 GiB; fill and sum (read only) over
+    exactly the AllGather's write and read volumes; and the fused Ring
+    AllGather fp32 P=8 (writes P bytes per byte read), in GB/s of bytes
+    moved."""
     import torch
     from collective_communication_algorithms_gb300 import _binding as B
     torch.cuda.set_device(0)
@@ -825,6 +847,9 @@ def sweep_hbm(args):
     src = a[:nb // 4 // P]
     dst = c.view(P, nb // 4 // P)
     cases = [("fill (write only), 1 GiB", lambda: c.fill_(1.0), nb),
+             ("fill (write only), 512 MiB: the AllGather's writes P n b",
+              lambda: c[:P * n].fill_(1.0), P * n * 4),
+             ("sum (read only), 64 MiB: the AllGather's reads n b", lambda: a[:n].sum(), n * 4),
              ("copy (read 1 GiB, write 1 GiB)", lambda: c.copy_(a), 2 * nb),
              ("broadcast copy (read 128 MiB, write 8 x 128 MiB)",
               lambda: dst.copy_(src.expand(P, -1)), nb + nb // P),
@@ -838,6 +863,7 @@ def sweep_hbm(args):
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        hold_device(args.steps)
         e0.record(s0)
         for _ in range(args.steps):
             fn()
