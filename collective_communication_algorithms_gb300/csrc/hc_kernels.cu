@@ -153,22 +153,23 @@ fused_allgather(const __grid_constant__ FusedParams p) {
 }
 
 // ---------------------------------------------------------------------------
-// TMA-staged AllGather.  One elected thread moves whole 16-byte-aligned tiles
+// TMA-staged AllGather.  One elected thread moves a 16-byte-aligned tile
 // between HBM and shared memory with the bulk-copy engine (cp.async.bulk),
-// completion tracked by mbarrier transaction counts, and bulk-stores every
-// tile from shared memory to all outputs.  Every wait on an mbarrier is
-// bounded: after kWaitLimitNs the block records HC_ERR_TIMEOUT in
-// hc_device_error, waits (again bounded) for its copies in flight and
-// returns.  (A TMA-staged reduce, one block per SM reducing from shared
-// memory, measured slower than the register path on GB300 for every
-// AllReduce / ReduceScatter shape tried: with 8 warps per SM the barrier
-// waits and the reduction could not hide behind the copies.)
+// completion tracked by an mbarrier transaction count, and bulk-stores it from
+// shared memory to all outputs.  Every wait on the mbarrier is bounded: after
+// kWaitLimitNs the block records HC_ERR_TIMEOUT in hc_device_error, waits
+// (again bounded) for its copy in flight and returns.  (A TMA-staged reduce,
+// one block per SM reducing from shared memory, measured slower than the
+// register path on GB300 for every AllReduce / ReduceScatter shape tried:
+// with 8 warps per SM the barrier waits and the reduction could not hide
+// behind the copies.)
 // ---------------------------------------------------------------------------
-// 32 KB tiles, 6 stages: 192 KB of shared memory, one block per SM.  Against
-// 8 KB x 8 (three blocks per SM) this measured 2-3 % faster for P = 8 and 14 %
-// faster for P = 32 (AllGather fp32, GB300), where each tile feeds 32 stores.
-constexpr int kAgTile = 32768;          // bytes per stage
-constexpr int kAgStages = 6;
+// One 32 KB tile per block, a block for every tile of every segment: blocks
+// are scheduled in index order, so the stores sweep each output from its
+// start.  On GB300 this beat one persistent block per SM streaming its tiles
+// through 6 stages (the previous design) by 9 % at P = 8 and 8 % at P = 32
+// (AllGather fp32, out of place), and up to 7 blocks share an SM.
+constexpr int kAgTile = 32768;          // bytes per block
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ int hc_device_error;
@@ -218,18 +219,12 @@ __device__ __forceinline__ void bulk_s2g(uintptr_t gdst, const void* smem_src, u
                  : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_read_1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-}
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
-// AllGather, TMA-staged: one thread streams the owner's segment through
-// shared memory in 32 KB tiles, each tile loaded once and bulk-stored to every
-// rank (the owner's own copy only when it is not already in place).
-// Broadcast: one segment owned by the root.
+// AllGather, TMA-staged: block (t, seg) loads tile t of the owner's segment
+// into shared memory once and bulk-stores it to every rank (the owner's own
+// copy only when it is not already in place).  Broadcast: one segment owned
+// by the root.
 template <int ES>
 __global__ void __launch_bounds__(32)
 fused_allgather_tma(const __grid_constant__ FusedParams p) {
@@ -243,58 +238,35 @@ fused_allgather_tma(const __grid_constant__ FusedParams p) {
     const bool skip_own = (p.skip_mask >> k) & 1ull;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (threadIdx.x == 0) {
-        uint64_t* full = (uint64_t*)(smem + (size_t)kAgStages * kAgTile);
-        const int64_t nbytes = nfull * 16;
-        const uintptr_t seg_off = (uintptr_t)sbeg * ES;
-        const int64_t ntiles = (nbytes + kAgTile - 1) / kAgTile;
-        const int64_t first = blockIdx.x, step = gridDim.x;
-        const int64_t mine = first < ntiles ? (ntiles - first + step - 1) / step : 0;
-        auto tile_bytes = [&](int64_t t) -> unsigned {
-            const int64_t b = nbytes - t * kAgTile;
-            return (unsigned)(b < kAgTile ? b : kAgTile);
-        };
-        auto issue_load = [&](int s, int64_t t) {
-            const unsigned tb = tile_bytes(t);
-            mbar_arrive_expect_tx(&full[s], tb);
-            bulk_g2s(smem + (size_t)s * kAgTile, p.src[k] + seg_off + (uintptr_t)t * kAgTile, tb, &full[s]);
-        };
-        for (int s = 0; s < kAgStages; s++) mbar_init(&full[s], 1);
+    if (threadIdx.x != 0) return;
+    uint64_t* full = (uint64_t*)(smem + kAgTile);
+    const int64_t nbytes = nfull * 16;
+    const int64_t t0 = (int64_t)blockIdx.x * kAgTile;
+    if (t0 < nbytes) {
+        const int64_t left = nbytes - t0;
+        const unsigned tb = (unsigned)(left < kAgTile ? left : kAgTile);
+        const uintptr_t off = (uintptr_t)sbeg * ES + (uintptr_t)t0;
+        mbar_init(full, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        for (int s = 0; s < kAgStages && s < mine; s++) issue_load(s, first + s * step);
-        bool aborted = false;
-        int64_t i = 0;
-        for (; i < mine; i++) {
-            const int s = (int)(i % kAgStages);
-            if (!mbar_wait_bounded(&full[s], (unsigned)((i / kAgStages) & 1))) {
-                aborted = true;
-                break;
-            }
-            const int64_t t = first + i * step;
-            const unsigned tb = tile_bytes(t);
-            const uintptr_t off = seg_off + (uintptr_t)t * kAgTile;
-            for (int r = 0; r < p.P; r++)
-                if (r != k || !skip_own) bulk_s2g(p.dst[r] + off, smem + (size_t)s * kAgTile, tb);
-            bulk_commit();
-            if (i >= 1) {
-                // the stores of tile i - 1 have read their stage: refill it
-                bulk_wait_read_1();
-                const int64_t nx = i - 1 + kAgStages;
-                if (nx < mine) issue_load((int)((i - 1) % kAgStages), first + nx * step);
-            }
-        }
-        bulk_wait_all();
-        if (aborted) {
+        mbar_arrive_expect_tx(full, tb);
+        bulk_g2s(smem, p.src[k] + off, tb, full);
+        if (!mbar_wait_bounded(full, 0)) {
             atomicExch(&hc_device_error, (int)HC_ERR_TIMEOUT);
-            for (int64_t j = i; j < mine && j < i + kAgStages; j++)
-                mbar_wait_bounded(&full[j % kAgStages], (unsigned)((j / kAgStages) & 1));
-        } else if (blockIdx.x == 0) {
-            for (int64_t x = sbeg + nfull * A; x < send_; x++) {
-                const uintptr_t xo = (uintptr_t)x * ES;
-                const uint32_t val = ld_elem<ES>(p.src[k] + xo);
-                for (int r = 0; r < p.P; r++)
-                    if (r != k || !skip_own) st_elem<ES>(p.dst[r] + xo, val);
-            }
+            mbar_wait_bounded(full, 0);  // the copy in flight must land before the block exits
+            return;
+        }
+        for (int r = 0; r < p.P; r++)
+            if (r != k || !skip_own) bulk_s2g(p.dst[r] + off, smem, tb);
+        bulk_commit();
+        bulk_wait_all();
+    }
+    if (blockIdx.x == 0) {
+        // ragged end of the segment (< 16 bytes)
+        for (int64_t x = sbeg + nfull * A; x < send_; x++) {
+            const uintptr_t xo = (uintptr_t)x * ES;
+            const uint32_t val = ld_elem<ES>(p.src[k] + xo);
+            for (int r = 0; r < p.P; r++)
+                if (r != k || !skip_own) st_elem<ES>(p.dst[r] + xo, val);
         }
     }
 }
@@ -477,60 +449,45 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     const int64_t seg_bytes = lay.L * es;
     void* args[] = {&p};
 
+    // Device buffers: one block per chunk of the segment (a 32 KB tile, or
+    // V x 256 vectors), so blocks are scheduled in index order and the stores
+    // sweep every output from its start.  On GB300 this measured 3 - 9 %
+    // faster than a persistent grid of a few blocks per SM striding over the
+    // segment, for every collective; plain stores from one-shot blocks
+    // reached 7.47 TB/s where grid-stride stores of the same bytes reached
+    // 6.3 TB/s.  Buffers in page-locked host memory keep a persistent grid
+    // (the host link, not HBM, bounds them).
     if (a.coll == HC_COLL_ALLGATHER || a.coll == HC_COLL_BROADCAST) {
-        // TMA path once every segment holds several tiles per block; buffers
-        // in host memory take the plain load / store path
+        // TMA path once every segment holds several tiles; buffers in host
+        // memory take the plain load / store path
         if (seg_bytes >= 16 * (int64_t)kAgTile && !a.host_buffers) {
             void* fn = es == 2 ? (void*)fused_allgather_tma<2> : (void*)fused_allgather_tma<4>;
-            const int smem = kAgStages * kAgTile + kAgStages * 8;
+            const int smem = kAgTile + 16;
             if (!allow_smem(fn, smem)) return cudaErrorInvalidValue;
-            int per_sm = 0;
-            cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, 32, smem);
-            if (e != cudaSuccess) return e;
             const int64_t tiles = (seg_bytes + kAgTile - 1) / kAgTile;
-            const int gx = (int)std::max<int64_t>(
-                1, std::min<int64_t>(tiles, (int64_t)sm_count * std::max(1, per_sm) / S));
-            return launch_pdl(fn, dim3(gx, S), dim3(32), args, smem, stream);
+            return launch_pdl(fn, dim3((unsigned)tiles, S), dim3(32), args, smem, stream);
         }
         void* fn = es == 2 ? (void*)fused_allgather<2> : (void*)fused_allgather<4>;
         const int64_t vecs = (lay.L + lay.A - 1) / lay.A;
         const int64_t want = std::max<int64_t>(1, (vecs + kFusedThreads - 1) / kFusedThreads);
-        const int gx = (int)std::min(want, std::max<int64_t>(1, (int64_t)sm_count * 4 / S));
-        return launch_pdl(fn, dim3(gx, S), dim3(kFusedThreads), args, 0, stream);
+        const int64_t gx = a.host_buffers ? std::min(want, std::max<int64_t>(1, (int64_t)sm_count * 4 / S)) : want;
+        return launch_pdl(fn, dim3((unsigned)gx, S), dim3(kFusedThreads), args, 0, stream);
     }
 
     const int COLL = a.coll == HC_COLL_ALLREDUCE ? 0 : 1;
-    // Register path.  Launch shape (vectors per thread V, blocks of 256
-    // threads per SM) chosen from measurements on GB300 (fraction of the
-    // measured copy bandwidth, reproducible to 0.5 % across processes):
-    //  ReduceScatter, or more than 16 ranks         V1, 8 per SM (0.93 - 0.94)
-    //  hierarchical AllReduce                       V1, 7 per SM (0.90)
-    //  AllReduce, 4-byte types                      V1, 6 per SM (0.95)
-    //  AllReduce, bf16 max / min                    V1, 4 per SM (0.91)
-    //  AllReduce, bf16 sum / prod, RHD              V2, 3 per SM (0.98)
-    //  AllReduce, bf16 sum / prod, Ring / Pipeline  V1, 5 per SM (0.97)
-    int V = 1, per_sm = 8;
-    if (COLL == 0 && a.algo == HC_ALGO_HIER) {
-        per_sm = 7;
-    } else if (COLL == 0 && a.P <= 16) {
-        if (es == 4) {
-            per_sm = 6;
-        } else if (a.op == HC_MAX || a.op == HC_MIN) {
-            per_sm = 4;
-        } else if (a.algo == HC_ALGO_RHD) {
-            V = 2;
-            per_sm = 3;
-        } else {
-            per_sm = 5;
-        }
-    }
+    // Register path, one block per chunk of V x 256 vectors.  V from
+    // measurements on GB300 (fraction of the measured copy bandwidth, one
+    // call, one-shot grids): bf16 sum / prod RHD AllReduce V2 (1.016, against
+    // 0.930 with V1); every other shape V1 (Ring fp32 AllReduce 0.97 - 1.00
+    // against 0.96 with V2).
+    int V = 1;
+    if (COLL == 0 && a.P <= 16 && es == 2 && a.algo == HC_ALGO_RHD &&
+        (a.op == HC_SUM || a.op == HC_PROD))
+        V = 2;
     // Page-locked host buffers: the host link (about 210 GB/s each way, 330
     // GB/s both ways at once on GB300 with Grace), not HBM, bounds the kernel;
     // 1 to 16 blocks per SM measured within 4 % of each other, 1 the fastest.
-    if (a.host_buffers) {
-        V = 1;
-        per_sm = 1;
-    }
+    if (a.host_buffers) V = 1;
     void* fn = pick_reduce(a.algo, COLL, a.dtype, a.op, V, a.P);
     if (!fn && V != 1) {  // shape not instantiated: one vector per thread
         V = 1;
@@ -539,8 +496,8 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     if (!fn) return cudaErrorInvalidValue;
     const int64_t vecs = (lay.L + lay.A - 1) / lay.A;
     const int64_t want = std::max<int64_t>(1, (vecs + (int64_t)V * kFusedThreads - 1) / ((int64_t)V * kFusedThreads));
-    const int gx = (int)std::min(want, std::max<int64_t>(1, (int64_t)sm_count * per_sm / S));
-    return launch_pdl(fn, dim3(gx, S), dim3(kFusedThreads), args, 0, stream);
+    const int64_t gx = a.host_buffers ? std::min(want, std::max<int64_t>(1, (int64_t)sm_count / S)) : want;
+    return launch_pdl(fn, dim3((unsigned)gx, S), dim3(kFusedThreads), args, 0, stream);
 }
 
 cudaError_t read_device_error(bool clear, int* status) {
