@@ -1,10 +1,12 @@
 // hc_api.cpp -- the C ABI of libhc (see include/hc.h): argument validation,
 // in-place detection, step-plan cache and dispatch to the kernels.
 #include <algorithm>
+#include <atomic>
 #include <cstddef>
 #include <cstring>
 #include <map>
 #include <memory>
+#include <mutex>
 #include <tuple>
 #include <vector>
 
@@ -95,13 +97,16 @@ hc_status_t check_device_accessible(const void* p) {
 }
 
 int sm_count_of_current_device() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];  // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 64 && cache[dev]) return cache[dev];
+    if (dev >= 0 && dev < 64) {
+        const int c = cache[dev].load(std::memory_order_relaxed);
+        if (c) return c;
+    }
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 64) cache[dev] = v;
+    if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
     return v;
 }
 
@@ -112,6 +117,8 @@ std::map<PlanKey, std::shared_ptr<const Plan>>& plan_cache() {
     static std::map<PlanKey, std::shared_ptr<const Plan>> m;
     return m;
 }
+// Guards plan_cache(): host threads may call the collectives concurrently.
+std::mutex g_plan_cache_mu;
 
 std::shared_ptr<const Plan> get_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root,
                                      int64_t n, hc_dtype_t dt, int64_t loop_bytes,
@@ -122,6 +129,7 @@ std::shared_ptr<const Plan> get_plan(hc_algo_t algo, hc_coll_t coll, int P, int 
         if (al.final_is_work[r]) m2 |= 1ull << r;
     }
     PlanKey key{(int)algo, (int)coll, P, p_intra, root, n, (int)dt, loop_bytes, m1, m2};
+    std::lock_guard<std::mutex> lock(g_plan_cache_mu);
     auto& cache = plan_cache();
     auto it = cache.find(key);
     if (it != cache.end()) return it->second;

@@ -24,6 +24,7 @@
 
 #include <algorithm>
 #include <cstring>
+#include <mutex>
 
 #include "hc_device.cuh"
 
@@ -305,10 +306,13 @@ cudaError_t launch_pdl(void* fn, dim3 grid, dim3 block, void** args, size_t smem
 
 // Raise a kernel's dynamic shared memory limit to at least `bytes` (the
 // attribute is per kernel, so remember the largest value set for each).
+std::mutex g_kernel_attr_mu;  // guards the per-kernel caches below
+
 bool allow_smem(void* fn, int bytes) {
     static void* fns[512];
     static int set[512];
     static int nfns = 0;
+    std::lock_guard<std::mutex> lock(g_kernel_attr_mu);
     int i = 0;
     while (i < nfns && fns[i] != fn) i++;
     if (i < nfns && set[i] >= bytes) return true;
@@ -342,6 +346,7 @@ int resident_blocks(void* fn) {
     static void* fns[256];
     static int val[256];
     static int nfns = 0;
+    std::lock_guard<std::mutex> lock(g_kernel_attr_mu);
     for (int i = 0; i < nfns; i++)
         if (fns[i] == fn) return val[i];
     int v = 0;

@@ -13,6 +13,8 @@
 // exits), and allocates nothing.
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "hc_internal.h"
 
 // The scratch itself.  Host code must never use this name as a device
@@ -24,18 +26,19 @@ namespace {
 
 // Device address of hc_static_scratch, per device, looked up on the first
 // call made with that device current.
-void* g_static_scratch_addr[hc::kMaxRanks] = {nullptr};
+std::atomic<void*> g_static_scratch_addr[hc::kMaxRanks];  // null-initialised (static storage)
 
 hc_status_t static_scratch_address(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess) return HC_ERR_CUDA;
     if (dev < 0 || dev >= hc::kMaxRanks) return HC_ERR_CUDA;
-    if (!g_static_scratch_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, hc_static_scratch) != cudaSuccess || !p) return HC_ERR_CUDA;
-        g_static_scratch_addr[dev] = p;
+    void* a = g_static_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        // two threads may both look it up; they store the same address
+        if (cudaGetSymbolAddress(&a, hc_static_scratch) != cudaSuccess || !a) return HC_ERR_CUDA;
+        g_static_scratch_addr[dev].store(a, std::memory_order_release);
     }
-    *out = g_static_scratch_addr[dev];
+    *out = a;
     return HC_OK;
 }
 

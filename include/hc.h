@@ -59,8 +59,12 @@
  *                I_t = X_(t,l) (+) X_(t,l+1) (+) ... (rotated from l),
  *                then I_{s+1} (+) I_{s+2} (+) ... (+) I_s around the
  *                inter-server ring (rank = server * ranks_per_server + local).
- *  - Not thread-safe: calls from several host threads must be serialised by
- *    the caller (the library keeps a small host-side cache).
+ *  - Thread-safe: host threads may call every entry point concurrently, on
+ *    the same or different streams.  The library's host-side caches (step
+ *    plans, per-kernel attributes, SM counts) are guarded by locks.  Calls
+ *    whose buffers overlap must still be ordered by the caller (one stream,
+ *    or events), and a graph object must not be used from two threads at
+ *    once.
  */
 #ifndef HC_H
 #define HC_H

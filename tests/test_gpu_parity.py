@@ -236,6 +236,59 @@ def test_concurrent_step_mode_calls_on_many_streams():
             assert same_bits(out[r].cpu().numpy(), Y[r], "float32"), (algo, r)
 
 
+def test_concurrent_calls_from_host_threads():
+    """Collectives issued from 6 host threads at once.  ctypes releases the
+    interpreter lock during each call, so the library's host code (argument
+    checks, step-plan cache, per-kernel attribute caches) runs concurrently.
+    Each thread has its own stream and buffers and mixes schedules, modes and
+    sizes, so plans are built and looked up concurrently; every result equals
+    the oracle's."""
+    import threading
+    from collective_communication_algorithms_gb300 import _binding as B
+    P, calls, nthreads = 8, 12, 6
+    jobs = [[] for _ in range(nthreads)]
+    for t in range(nthreads):
+        for i in range(calls):
+            j = t * calls + i
+            algo = ("ring", "rhd", "pipeline")[j % 3]
+            mode = ("fused", "step")[(j // 3) % 2]
+            n = 4099 + 4 * (j % 5)  # a few sizes: plans shared and not shared between threads
+            X = hc_inputs.gradients_f32(P, n, seed=5000 + j)
+            dev = [torch.from_numpy(X[r].copy()).cuda() for r in range(P)]  # one allocation per rank
+            out = [torch.empty_like(d) for d in dev]
+            jobs[t].append((algo, mode, n, X, dev, out))
+    torch.cuda.synchronize()
+    errors = []
+    start = threading.Barrier(nthreads)
+
+    def worker(t):
+        try:
+            s = torch.cuda.Stream()
+            start.wait()
+            for algo, mode, n, X, dev, out in jobs[t]:
+                opts = B.make_opts(mode, ranks_per_server=2 if algo == "pipeline" else 1)
+                B.hc_allreduce([d.data_ptr() for d in dev], [o.data_ptr() for o in out],
+                               P, n, "float32", "sum", algo, opts, s.cuda_stream)
+            s.synchronize()
+        except Exception as e:  # reported by the main thread
+            errors.append((t, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(nthreads)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=300)
+    assert not errors, errors
+    assert all(not th.is_alive() for th in threads)
+    torch.cuda.synchronize()
+    assert B.hc_device_status() == 0
+    for t in range(nthreads):
+        for algo, mode, n, X, dev, out in jobs[t]:
+            Y = O.replay(algo, "allreduce", X, "sum", "float32", p_intra=2 if algo == "pipeline" else 1)
+            for r in range(P):
+                assert same_bits(out[r].cpu().numpy(), Y[r], "float32"), (t, algo, mode, n, r)
+
+
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_tma_staged_paths(algo, dtype):

@@ -580,3 +580,42 @@ def test_cost_model_selector():
     assert B.hc_select_algo("allreduce", 8, 1024, "float32", "step")[0] == "rhd"
     assert B.hc_select_algo("allreduce", 16, 256, "float32", "step")[0] == "rhd"
     assert B.hc_select_algo("broadcast", 8, 1024, "float32", "step")[0] == "rhd"
+
+
+def test_plan_cache_under_concurrent_host_threads():
+    """Step-mode collectives validated from 8 host threads at once (graph
+    adds: each builds or looks up its step plan in the library's shared plan
+    cache, nothing is launched).  ctypes releases the interpreter lock during
+    each call, so the cache is really used concurrently; enough distinct
+    shapes pass through it to make it clear and refill.  Every add succeeds
+    and no thread sees an error."""
+    import threading
+    nthreads, per_thread = 8, 60
+    errors = []
+    start = threading.Barrier(nthreads)
+
+    def worker(t):
+        try:
+            g = B.Graph()
+            start.wait()
+            for i in range(per_thread):
+                j = t * per_thread + i
+                algo = ("ring", "rhd", "pipeline")[j % 3]
+                P = (4, 8, 12)[(j // 3) % 3]
+                n = 1024 + 4 * (j % 97)
+                opts = B.make_opts("step", ranks_per_server=2 if algo == "pipeline" else 1)
+                A = fake(P, base=BASE + (2 * i) * 64 * MB)
+                C = fake(P, base=BASE + (2 * i + 1) * 64 * MB)
+                g.add_allreduce(A, C, P, n, "float32", "sum", algo, opts)
+            assert g.info()["collectives"] == per_thread
+            g.close()
+        except Exception as e:  # reported by the main thread
+            errors.append((t, repr(e)))
+
+    threads = [threading.Thread(target=worker, args=(t,)) for t in range(nthreads)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=300)
+    assert not errors, errors
+    assert all(not th.is_alive() for th in threads)
