@@ -2,8 +2,9 @@
 // translation units of libhc: the element-wise operators (int32 wrap, fp32
 // RNE without contraction or flush to zero, bf16 widened to fp32 and rounded
 // back with cvt.rn.bf16x2.f32, max/min by IEEE totalOrder keys), 16-byte
-// memory access, and the fused register-path kernel template with the
-// association order of every schedule.  Internal; not installed.
+// memory access, bulk copies with bounded mbarrier waits, and the fused
+// kernel templates (register path and TMA-staged) with the association order
+// of every schedule.  Internal; not installed.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -24,6 +25,7 @@ struct FusedParams {
     int stages;                // TMA kernels: pipeline depth
     int owner;                 // Broadcast: the root owns the single segment (-1: segment k's owner is k)
     unsigned long long skip_mask;  // AllGather / Broadcast: ranks whose data is already in place
+    int* err;                  // device address of the library's error flag (HC_ERR_TIMEOUT on a wait that gave up)
 };
 
 // Register-path fused kernels, one translation unit per algorithm.
@@ -34,6 +36,11 @@ void* pick_fused_ring(int coll, hc_dtype_t dt, hc_op_t op, int V);
 void* pick_fused_rhd(int coll, hc_dtype_t dt, hc_op_t op, int V, bool large);
 void* pick_fused_pipe(int coll, hc_dtype_t dt, hc_op_t op, int V);
 void* pick_fused_hier(int coll, hc_dtype_t dt, hc_op_t op, int V);
+// TMA-staged fused kernels (fused_reduce_tma) of the same schedules.
+void* pick_fused_ring_tma(int coll, hc_dtype_t dt, hc_op_t op);
+void* pick_fused_rhd_tma(int coll, hc_dtype_t dt, hc_op_t op, bool large);
+void* pick_fused_pipe_tma(int coll, hc_dtype_t dt, hc_op_t op);
+void* pick_fused_hier_tma(int coll, hc_dtype_t dt, hc_op_t op);
 
 namespace {
 
@@ -129,6 +136,59 @@ __device__ __forceinline__ void st_vec(uintptr_t p, const uint4& v) { *(uint4*)p
 // streaming variants for data touched once by the fused kernels
 __device__ __forceinline__ uint4 ld_stream(uintptr_t p) { return __ldcs((const uint4*)p); }
 __device__ __forceinline__ void st_stream(uintptr_t p, const uint4& v) { __stcs((uint4*)p, v); }
+
+// ---------------------------------------------------------------------------
+// bulk copies (cp.async.bulk) and mbarriers with bounded waits
+// ---------------------------------------------------------------------------
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ unsigned smem_addr(const void* p) {
+    return (unsigned)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint64_t* m, unsigned count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(m)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* m, unsigned bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(m)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* m, unsigned parity) {
+    unsigned ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_addr(m)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Poll an mbarrier phase for at most kWaitLimitNs.
+__device__ bool mbar_wait_bounded(uint64_t* m, unsigned parity) {
+    const unsigned long long t0 = global_ns();
+    while (!mbar_try_wait(m, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, uintptr_t gsrc, unsigned bytes, uint64_t* m) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_addr(m))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(uintptr_t gdst, const void* smem_src, unsigned bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+                 "r"(smem_addr(smem_src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 
 template <hc_dtype_t DT>
 struct DT_ {
@@ -350,6 +410,83 @@ fused_reduce(const __grid_constant__ FusedParams p) {
     if (blockIdx.x == 0 && threadIdx.x == 0) ragged_tail<ALGO, COLL, DT, OP>(p, k, sbeg + nfull * A, send_);
 }
 
+
+// AllReduce (COLL = 0) and ReduceScatter (COLL = 1), TMA-staged: block
+// (t, k) moves tile t of segment k (kTmaTile bytes, 16 per thread) of every
+// rank into shared memory with one bulk copy per rank, all completing on one
+// mbarrier; then each thread reduces its 16-byte vector from shared memory
+// in the schedule's order and stores it to every output (AllReduce) or to the
+// owner's (ReduceScatter).  Shared memory: P tiles, so P <= kTmaMaxRanks.
+// The mbarrier wait is bounded: on expiry the block records HC_ERR_TIMEOUT in
+// *p.err, waits (again bounded) for its copies in flight and returns.
+constexpr int kTmaThreads = 128;
+constexpr int kTmaTile = kTmaThreads * 16;  // bytes per rank per block
+constexpr int kTmaMaxRanks = 32;            // 64 KB of tiles per block
+
+template <hc_algo_t ALGO, int COLL, hc_dtype_t DT, hc_op_t OP>
+__global__ void __launch_bounds__(kTmaThreads)
+fused_reduce_tma(const __grid_constant__ FusedParams p) {
+    constexpr int ES = DT_<DT>::ES;
+    constexpr int A = DT_<DT>::A;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int k = blockIdx.y;
+    const int64_t sbeg = (int64_t)k * p.L;
+    if (sbeg >= p.n) return;  // empty trailing segment
+    const int64_t send_ = (sbeg + p.L < p.n) ? sbeg + p.L : p.n;
+    const int64_t nfull = (send_ - sbeg) / A;
+    const int64_t nbytes = nfull * 16;
+    const int64_t t0 = (int64_t)blockIdx.x * kTmaTile;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (t0 < nbytes) {
+        const int64_t left = nbytes - t0;
+        const unsigned tb = (unsigned)(left < kTmaTile ? left : kTmaTile);
+        const uintptr_t off = (uintptr_t)sbeg * ES + (uintptr_t)t0;
+        uint64_t* full = (uint64_t*)(smem + (size_t)p.P * kTmaTile);
+        if (threadIdx.x == 0) {
+            mbar_init(full, 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            mbar_arrive_expect_tx(full, tb * (unsigned)p.P);
+            for (int r = 0; r < p.P; r++) bulk_g2s(smem + (size_t)r * kTmaTile, p.src[r] + off, tb, full);
+        }
+        __syncthreads();  // the mbarrier is initialised before anyone polls it
+        if (!mbar_wait_bounded(full, 0)) {
+            atomicExch(p.err, (int)HC_ERR_TIMEOUT);
+            mbar_wait_bounded(full, 0);  // the copies in flight must land before the block exits
+            return;
+        }
+        const unsigned vo = threadIdx.x * 16u;
+        if (vo < tb) {
+            auto load = [&](int r) -> uint4 { return *(const uint4*)(smem + (size_t)r * kTmaTile + vo); };
+            const uint4 acc = segment_reduce<ALGO, DT, OP, uint4>(p, k, load);
+            if (COLL == 0) {
+                for (int r = 0; r < p.P; r++) st_stream(p.dst[r] + off + vo, acc);
+            } else {
+                st_stream(p.dst[k] + off + vo, acc);
+            }
+        }
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) ragged_tail<ALGO, COLL, DT, OP>(p, k, sbeg + nfull * A, send_);
+}
+
+// Kernel table of the TMA-staged kernels of one algorithm.
+template <hc_algo_t ALGO, int COLL, hc_dtype_t DT>
+void* pick_tma_op(hc_op_t op) {
+    switch (op) {
+    case HC_SUM: return (void*)fused_reduce_tma<ALGO, COLL, DT, HC_SUM>;
+    case HC_PROD: return (void*)fused_reduce_tma<ALGO, COLL, DT, HC_PROD>;
+    case HC_MAX: return (void*)fused_reduce_tma<ALGO, COLL, DT, HC_MAX>;
+    default: return (void*)fused_reduce_tma<ALGO, COLL, DT, HC_MIN>;
+    }
+}
+template <hc_algo_t ALGO>
+void* pick_tma(int coll, hc_dtype_t dt, hc_op_t op) {
+    switch (dt) {
+    case HC_INT32: return coll == 0 ? pick_tma_op<ALGO, 0, HC_INT32>(op) : pick_tma_op<ALGO, 1, HC_INT32>(op);
+    case HC_FLOAT32: return coll == 0 ? pick_tma_op<ALGO, 0, HC_FLOAT32>(op) : pick_tma_op<ALGO, 1, HC_FLOAT32>(op);
+    default: return coll == 0 ? pick_tma_op<ALGO, 0, HC_BFLOAT16>(op) : pick_tma_op<ALGO, 1, HC_BFLOAT16>(op);
+    }
+}
 
 // Kernel table of one algorithm: the register-path kernels for every dtype,
 // op, collective and (where instantiated) vectors per thread.

@@ -9,12 +9,15 @@
 //               and the Pipeline article's LocalCopy, with the HCOMM transfer
 //               replaced by a load from the peer's buffer.
 //  fused_*      (fused mode): one launch per collective; each thread takes a
-//               16-byte vector of a segment, loads it from every rank, reduces
+//               16-byte vector of a segment, reads it from every rank, reduces
 //               in registers in exactly the association order the schedule
 //               implies (Ring chain, RHD fold + pairwise tree, Pipeline
 //               intra-server chain then inter-server chain) and stores it to
-//               every output.  Minimum traffic: AllReduce reads and writes
-//               P n b bytes.
+//               every output.  Up to 32 ranks the inputs are staged in shared
+//               memory by bulk copies (fused_reduce_tma, hc_device.cuh); the
+//               AllGather / Broadcast bulk-stores 32 KB tiles from shared
+//               memory.  Minimum traffic: AllReduce reads and writes P n b
+//               bytes.
 //
 // Arithmetic (must match the reduction semantics in hc.h bit for bit):
 //  int32 wrap; fp32 IEEE RNE via __fadd_rn / __fmul_rn (no contraction, no
@@ -23,6 +26,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 
@@ -159,11 +163,7 @@ fused_allgather(const __grid_constant__ FusedParams p) {
 // completion tracked by an mbarrier transaction count, and bulk-stores it from
 // shared memory to all outputs.  Every wait on the mbarrier is bounded: after
 // kWaitLimitNs the block records HC_ERR_TIMEOUT in hc_device_error, waits
-// (again bounded) for its copy in flight and returns.  (A TMA-staged reduce,
-// one block per SM reducing from shared memory, measured slower than the
-// register path on GB300 for every AllReduce / ReduceScatter shape tried:
-// with 8 warps per SM the barrier waits and the reduction could not hide
-// behind the copies.)
+// (again bounded) for its copy in flight and returns.
 // ---------------------------------------------------------------------------
 // One 32 KB tile per block, a block for every tile of every segment: blocks
 // are scheduled in index order, so the stores sweep each output from its
@@ -171,56 +171,7 @@ fused_allgather(const __grid_constant__ FusedParams p) {
 // through 6 stages (the previous design) by 9 % at P = 8 and 8 % at P = 32
 // (AllGather fp32, out of place), and up to 7 blocks share an SM.
 constexpr int kAgTile = 32768;          // bytes per block
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;
-
 __device__ int hc_device_error;
-
-__device__ __forceinline__ unsigned smem_addr(const void* p) {
-    return (unsigned)__cvta_generic_to_shared(p);
-}
-__device__ __forceinline__ void mbar_init(uint64_t* m, unsigned count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(m)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* m, unsigned bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(m)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* m, unsigned parity) {
-    unsigned ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(smem_addr(m)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-__device__ __forceinline__ unsigned long long global_ns() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-// Poll an mbarrier phase for at most kWaitLimitNs.
-__device__ bool mbar_wait_bounded(uint64_t* m, unsigned parity) {
-    const unsigned long long t0 = global_ns();
-    while (!mbar_try_wait(m, parity))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
-    return true;
-}
-__device__ __forceinline__ void bulk_g2s(void* smem_dst, uintptr_t gsrc, unsigned bytes, uint64_t* m) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            smem_addr(smem_dst)),
-        "l"(gsrc), "r"(bytes), "r"(smem_addr(m))
-        : "memory");
-}
-__device__ __forceinline__ void bulk_s2g(uintptr_t gdst, const void* smem_src, unsigned bytes) {
-    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
-                 "r"(smem_addr(smem_src)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // AllGather, TMA-staged: block (t, seg) loads tile t of the owner's segment
 // into shared memory once and bulk-stores it to every rank (the owner's own
@@ -283,6 +234,32 @@ void* pick_reduce(hc_algo_t algo, int coll, hc_dtype_t dt, hc_op_t op, int V, in
     case HC_ALGO_HIER: return pick_fused_hier(coll, dt, op, V);
     default: return pick_fused_pipe(coll, dt, op, V);
     }
+}
+
+// TMA-staged fused reduce of (algo, collective, dtype, op).
+void* pick_reduce_tma(hc_algo_t algo, int coll, hc_dtype_t dt, hc_op_t op, int P) {
+    switch (algo) {
+    case HC_ALGO_RING: return pick_fused_ring_tma(coll, dt, op);
+    case HC_ALGO_RHD: return pick_fused_rhd_tma(coll, dt, op, P >= 16);
+    case HC_ALGO_HIER: return pick_fused_hier_tma(coll, dt, op);
+    default: return pick_fused_pipe_tma(coll, dt, op);
+    }
+}
+
+// Device address of hc_device_error on the current device (looked up once
+// per device).
+int* device_error_flag() {
+    static std::atomic<int*> addr[64];  // null-initialised (static storage)
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    int* a = addr[dev].load(std::memory_order_acquire);
+    if (!a) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, hc_device_error) != cudaSuccess) return nullptr;
+        a = (int*)p;
+        addr[dev].store(a, std::memory_order_release);
+    }
+    return a;
 }
 
 // Launch with programmatic stream serialization: the kernel waits for the
@@ -480,6 +457,25 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     }
 
     const int COLL = a.coll == HC_COLL_ALLREDUCE ? 0 : 1;
+    // TMA-staged path: device buffers and P <= kTmaMaxRanks (P tiles of
+    // shared memory per block), one block per kTmaTile bytes of a segment.
+    // Against the register path on GB300 (fraction of the measured copy
+    // bandwidth, same call): Pipeline fp32 4x8 1.007 vs 0.953, hierarchical
+    // 0.994 vs 0.930, Ring ReduceScatter fp32 1.010 vs 0.964; Ring fp32 and
+    // bf16 and RHD bf16 sum AllReduce within 0.2 %; RHD bf16 max 0.989 vs
+    // 1.005, so bf16 max / min up to 16 ranks keep the register path.
+    const bool bf16_maxmin = es == 2 && (a.op == HC_MAX || a.op == HC_MIN);
+    if (!a.host_buffers && a.P <= kTmaMaxRanks && !(bf16_maxmin && a.P <= 16)) {
+        void* fn = pick_reduce_tma(a.algo, COLL, a.dtype, a.op, a.P);
+        if (fn) {
+            p.err = device_error_flag();
+            if (!p.err) return cudaErrorInvalidValue;
+            const int smem = a.P * kTmaTile + 16;
+            if (!allow_smem(fn, smem)) return cudaErrorInvalidValue;
+            const int64_t tiles = std::max<int64_t>(1, (seg_bytes + kTmaTile - 1) / kTmaTile);
+            return launch_pdl(fn, dim3((unsigned)tiles, S), dim3(kTmaThreads), args, smem, stream);
+        }
+    }
     // Register path, one block per chunk of V x 256 vectors.  V from
     // measurements on GB300 (fraction of the measured copy bandwidth, one
     // call, one-shot grids): bf16 sum / prod RHD AllReduce V2 (1.016, against
