@@ -290,6 +290,24 @@ def test_concurrent_calls_from_host_threads():
 
 
 @pytest.mark.parametrize("algo", ALGOS)
+@pytest.mark.parametrize("dtype", ("float32", "bfloat16"))
+def test_fused_around_the_tma_rank_limit(algo, dtype):
+    """Fused AllReduce and ReduceScatter with 17, 20, 32 and 33 ranks: the
+    TMA-staged kernel up to 32 ranks (at 32 its P shared-memory tiles fill
+    64 KB; RHD's 16-and-more-rank tree), the register path at 33.  Several
+    tiles per segment and a ragged end; bit for bit against the oracle's
+    replay, sum and max, in place and out of place."""
+    for P in (17, 20, 32, 33):
+        pin = intra_for(algo, P)
+        n = P * 2048 + 13
+        for op in ("sum", "max"):
+            X = inputs(dtype, P, n, seed=P * 13 + 5, op=op)
+            for in_place in (False, True):
+                check("allreduce", algo, X, dtype, op, "fused", in_place, pin)
+                check("reducescatter", algo, X, dtype, op, "fused", in_place, pin)
+
+
+@pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_tma_staged_paths(algo, dtype):
     """Segments long enough for the TMA-staged AllGather (at least 16 tiles of
