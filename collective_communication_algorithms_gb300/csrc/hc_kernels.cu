@@ -40,6 +40,12 @@ namespace {
 // ---------------------------------------------------------------------------
 constexpr int kStepThreads = 256;
 constexpr int kStepBatch = 8;  // input loads in flight per vector
+// Vectors per thread per loop pass for single-input items (a copy, or
+// acc (+) one input: every Ring and RHD step, the inter-server steps): all
+// their loads are issued before any is reduced.  On GB300 two measured
+// 0.96 of the copy bandwidth for the Ring AllReduce fp32 step mode against
+// 0.83 with one, and the hierarchical steps 0.91 against 0.87.
+constexpr int kStepUnroll = 2;
 
 // BATCH: input loads issued before reducing (1 for launches whose items
 // have at most two inputs, where 8 blocks per SM give the loads in flight;
@@ -73,6 +79,34 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
         if (hi > send_) hi = send_;
         const int64_t lo = sbeg + p.lo;
         for (int64_t e = lo + t0 * A; e < hi; e += nthreads * A) {
+            if (BATCH == 1 && I.in_cnt == 1 && e + (kStepUnroll - 1) * nthreads * A + A <= hi) {
+                // kStepUnroll full vectors, nthreads * A elements apart
+                uintptr_t o[kStepUnroll];
+                uint4 x[kStepUnroll];
+                const uintptr_t ib = p.base[I.in_loc][I.in_base + I.in_rot];
+#pragma unroll
+                for (int u = 0; u < kStepUnroll; u++) {
+                    o[u] = (uintptr_t)(e + u * nthreads * A) * ES;
+                    x[u] = ld_vec(ib + o[u]);
+                }
+                if (I.acc_rank >= 0) {
+                    const uintptr_t ab = p.base[I.acc_loc][I.acc_rank];
+                    uint4 a[kStepUnroll];
+#pragma unroll
+                    for (int u = 0; u < kStepUnroll; u++) a[u] = ld_vec(ab + o[u]);
+#pragma unroll
+                    for (int u = 0; u < kStepUnroll; u++) x[u] = vop<DT, OP>(a[u], x[u]);
+                }
+                int oo = I.out_rot;
+                for (int j = 0; j < I.out_cnt; j++) {
+                    const uintptr_t ob = p.base[I.out_loc][I.out_base + oo];
+#pragma unroll
+                    for (int u = 0; u < kStepUnroll; u++) st_vec(ob + o[u], x[u]);
+                    if (++oo == I.out_mod) oo = 0;
+                }
+                e += (kStepUnroll - 1) * nthreads * A;  // the loop step adds the last stride
+                continue;
+            }
             const uintptr_t off = (uintptr_t)e * ES;
             if (e + A <= hi) {
                 // issue the accumulator's and up to BATCH inputs' loads
