@@ -542,7 +542,7 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
     // kernels reach (measured on GB300; step kernels launched with programmatic
     // stream serialization, fused kernels TMA-staged, one block per tile)
     const double kHostCallUs = 3.5, kHostLaunchUs = 2.3, kDeviceStepUs = 3.0;
-    const double kBandwidth = 6800e9, kStepFrac = 0.83, kFusedFrac = 1.0;
+    const double kBandwidth = 6800e9, kStepFrac = 0.9, kFusedFrac = 1.0;
     if (!out_algo || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
     if (mode != HC_MODE_FUSED && mode != HC_MODE_STEP) return HC_ERR_INVALID_ARG;
     if (P < 1 || P > kMaxRanks) return HC_ERR_INVALID_ARG;

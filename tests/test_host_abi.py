@@ -562,7 +562,7 @@ def test_cost_model_selector():
         st, _ = B.hc_schedule_stats(algo, coll, P, n, "float32", rps, 0)
         L = st["launches_step"] if mode == "step" else st["launches_fused"]
         by = st["step_bytes"] if mode == "step" else st["fused_bytes"]
-        f = 0.83 if mode == "step" else 1.0
+        f = 0.9 if mode == "step" else 1.0
         return max(3.5 + L * 2.3, L * 3.0 + by / (f * 6800e9) * 1e6)
     for coll in ("allreduce", "reducescatter", "allgather"):
         for P, rps in ((2, 1), (5, 1), (8, 1), (12, 4), (16, 4), (32, 8), (64, 8)):
