@@ -385,7 +385,7 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
  *           launches * alpha_dev + bytes / (f * B))
  * with launches and bytes (step or fused mode) from hc_schedule_stats and
  * c_host = 3.5 us per call, alpha_host = 2.3 us per launch, alpha_dev =
- * 3.0 us per dependent launch, f = 0.83 (step) / 0.93 (fused), B = 6800 GB/s,
+ * 3.0 us per dependent launch, f = 0.9 (step) / 1.0 (fused), B = 6800 GB/s,
  * all measured on GB300.  Candidates: Ring and RHD;
  * Pipeline and, for an AllReduce, the hierarchical AllReduce when
  * ranks_per_server > 1 divides P.  On a tie the earlier candidate wins (Ring,
