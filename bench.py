@@ -147,6 +147,21 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
+def l2_note(coll, P, rank_bytes):
+    """How the timed steps avoid reusing the 129 MB L2: the inputs (P n b for
+    AllReduce and ReduceScatter, n b for AllGather) are larger than it, or
+    every step writes more than it (AllGather: P n b), which evicts the
+    inputs between steps."""
+    l2 = 129 << 20
+    inputs = rank_bytes if coll == "allgather" else P * rank_bytes
+    if inputs > l2:
+        return "inputs (%d MiB) larger than the 129 MB L2; no flush" % (inputs >> 20)
+    if coll == "allgather" and P * rank_bytes > l2:
+        return ("inputs %d MiB; every step writes %d MiB (more than the 129 MB L2), which evicts "
+                "them between steps; no other flush" % (inputs >> 20, (P * rank_bytes) >> 20))
+    return "L2-resident (hot-cache latency regime)"
+
+
 def hold_device(steps):
     """Queue a spin kernel on the current stream ahead of a timed region, so
     that the host enqueues all `steps` calls before the device starts them
@@ -451,8 +466,7 @@ def run_ours(args, w):
         "config": {"workload": w["desc"], "algo": w["algo"], "collective": w["coll"], "P": P,
                    "elements_per_rank": n, "mode": w["mode"], "op": w["op"],
                    "ranks_per_server": w["p_intra"], "max_loop_bytes": w["loop_bytes"],
-                   "l2": "inputs (%d MiB) larger than the 129 MB L2; no flush" % (P * n * b >> 20)
-                   if P * n * b > (129 << 20) else "L2-resident (hot-cache latency regime)",
+                   "l2": l2_note(w["coll"], P, n * b),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "clock_window": "1.5 s sustained run of the same step + the timed steps"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
