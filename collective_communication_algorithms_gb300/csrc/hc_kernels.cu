@@ -316,20 +316,27 @@ cudaError_t launch_pdl(void* fn, dim3 grid, dim3 block, void** args, size_t smem
 }
 
 // Raise a kernel's dynamic shared memory limit to at least `bytes` (the
-// attribute is per kernel, so remember the largest value set for each).
+// attribute is per kernel and device, so remember the largest value set for
+// each pair).
 std::mutex g_kernel_attr_mu;  // guards the per-kernel caches below
 
 bool allow_smem(void* fn, int bytes) {
     static void* fns[512];
+    static int devs[512];
     static int set[512];
     static int nfns = 0;
-    std::lock_guard<std::mutex> lock(g_kernel_attr_mu);
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    std::lock_guard<std::mutex> lock(g_kernel_attr_mu);  // the attribute is per device
     int i = 0;
-    while (i < nfns && fns[i] != fn) i++;
+    while (i < nfns && (fns[i] != fn || devs[i] != dev)) i++;
     if (i < nfns && set[i] >= bytes) return true;
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
         return false;
-    if (i == nfns && nfns < 512) fns[nfns++] = fn;
+    if (i == nfns && nfns < 512) {
+        fns[nfns] = fn;
+        devs[nfns++] = dev;
+    }
     if (i < nfns) set[i] = bytes;
     return true;
 }
