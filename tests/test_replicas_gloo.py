@@ -68,3 +68,14 @@ def test_reference_arm_ranks_other_than_0_exit_without_work(monkeypatch):
         raise AssertionError("rank 1 must not run the oracle")
     monkeypatch.setattr(bench, "ParallelOracle", no_oracle)
     assert bench.run_reference(None, bench.WORKLOADS["ring_fp32_p8"]) is None
+
+
+def test_l2_note_names_the_case_that_applies():
+    """AllReduce / ReduceScatter inputs (P n b) larger than the 129 MB L2;
+    an AllGather whose inputs fit but whose outputs (P n b) do not; and the
+    L2-resident latency regime."""
+    assert bench.l2_note("allreduce", 8, 64 << 20).startswith("inputs (512 MiB) larger")
+    assert bench.l2_note("reducescatter", 32, 32 << 20).startswith("inputs (1024 MiB) larger")
+    ag = bench.l2_note("allgather", 8, 64 << 20)
+    assert ag.startswith("inputs 64 MiB; every step writes 512 MiB")
+    assert bench.l2_note("allreduce", 8, 16 << 10) == "L2-resident (hot-cache latency regime)"
