@@ -66,7 +66,8 @@ EXPORTS = ("hc_allreduce", "hc_reduce_scatter", "hc_reduce_scatter_static_scratc
            "hc_graph_add_broadcast", "hc_graph_build",
            "hc_graph_launch", "hc_graph_info", "hc_graph_destroy",
            "hc_num_segments", "hc_scratch_bytes", "hc_schedule_stats", "hc_step_plan",
-           "hc_select_algo", "hc_device_status", "hc_last_cuda_error", "hc_status_string",
+           "hc_select_algo", "hc_device_status", "hc_test_expire_waits", "hc_last_cuda_error",
+           "hc_status_string",
            "hc_version")
 
 _lib = None
@@ -135,6 +136,8 @@ def lib():
         L.hc_last_cuda_error.restype = ctypes.c_char_p
         L.hc_device_status.argtypes = [i32]
         L.hc_device_status.restype = i32
+        L.hc_test_expire_waits.argtypes = [i32]
+        L.hc_test_expire_waits.restype = i32
         L.hc_status_string.argtypes = [i32]
         L.hc_status_string.restype = ctypes.c_char_p
         L.hc_version.argtypes = []
@@ -156,12 +159,19 @@ def _check(status, where):
 
 
 def _ptr_array(ptrs):
-    if ptrs is None:
-        return None
+    if ptrs is None or isinstance(ptrs, ctypes.Array):
+        return ptrs  # None, or an array built once with ptr_array() and reused
     arr = (ctypes.c_void_p * len(ptrs))()
     for i, p in enumerate(ptrs):
         arr[i] = int(p) if p else None
     return arr
+
+
+def ptr_array(ptrs):
+    """A ctypes array of the pointers, which every hc_* function accepts in
+    place of a list: callers that issue many calls on the same buffers build
+    it once and skip the per-call conversion."""
+    return _ptr_array(list(ptrs))
 
 
 def make_opts(mode="fused", ranks_per_server=1, max_loop_bytes=0, scratch=0, scratch_bytes=0,
@@ -351,6 +361,12 @@ class Graph:
             self.close()
         except Exception:
             pass
+
+
+def hc_test_expire_waits(enable):
+    """Test hook: TMA-staged fused kernels launched while enabled give up their
+    first shared-memory barrier wait after 1 ms and report HC_ERR_TIMEOUT."""
+    _check(lib().hc_test_expire_waits(1 if enable else 0), "hc_test_expire_waits")
 
 
 def hc_version():

@@ -17,7 +17,8 @@ OUT = os.path.join(HERE, "_lib")
 LIB = os.path.join(OUT, "libhc.so")
 ARCHIVE = os.path.join(OUT, "libhc.a")
 SOURCES = ["hc_kernels.cu", "hc_fused_ring.cu", "hc_fused_rhd.cu", "hc_fused_pipe.cu",
-           "hc_fused_hier.cu", "hc_sched.cpp", "hc_api.cpp", "hc_graph.cpp", "hc_static_scratch.cu"]
+           "hc_fused_hier.cu", "hc_sched.cpp", "hc_api.cpp", "hc_graph.cpp", "hc_static_scratch.cu",
+           "hc_trace.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

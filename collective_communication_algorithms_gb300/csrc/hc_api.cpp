@@ -97,16 +97,16 @@ hc_status_t check_device_accessible(const void* p) {
 }
 
 int sm_count_of_current_device() {
-    static std::atomic<int> cache[64];  // zero-initialised (static storage)
+    static std::atomic<int> cache[kMaxDevices];  // zero-initialised (static storage)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 64) {
+    if (dev >= 0 && dev < kMaxDevices) {
         const int c = cache[dev].load(std::memory_order_relaxed);
         if (c) return c;
     }
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (dev >= 0 && dev < 64) cache[dev].store(v, std::memory_order_relaxed);
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(v, std::memory_order_relaxed);
     return v;
 }
 
@@ -137,6 +137,7 @@ std::shared_ptr<const Plan> get_plan(hc_algo_t algo, hc_coll_t coll, int P, int 
     auto plan = std::make_shared<Plan>();
     if (!build_plan(algo, coll, P, p_intra, root, n, dt, loop_bytes, al, plan.get())) return nullptr;
     cache.emplace(key, plan);
+    log_plan(algo, coll, P, p_intra, n, dt, loop_bytes, *plan);
     return plan;
 }
 
@@ -298,11 +299,13 @@ hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, 
 // Launch a prepared call on a stream.
 hc_status_t execute(const Prepared& c, cudaStream_t stream) {
     if (c.empty) return HC_OK;
+    const TraceRange range(c.coll, trace_category(c.algo, c.mode), (uint64_t)c.count);
     const int sms = sm_count_of_current_device();
     if (sms <= 0) return cuda_status(cudaErrorNoDevice);
     const int es = elem_bytes(c.dtype);
     const Layout& own = c.lay;
     if (c.mode == HC_MODE_FUSED) {
+        log_fused(c);
         const void* sp[kMaxRanks];
         void* rp[kMaxRanks];
         for (int r = 0; r < c.P; r++) {
@@ -349,7 +352,7 @@ hc_status_t execute(const Prepared& c, cudaStream_t stream) {
             base[LOC_FINAL][r] = d;
         }
     }
-    return cuda_status(launch_step(*c.plan, c.P, c.dtype, c.op, base, stream, sms));
+    return cuda_status(launch_step(*c.plan, c.P, c.dtype, c.op, base, stream, sms, c.host_buffers));
 }
 
 bool conflicts(const Prepared& a, const Prepared& b) {
@@ -583,6 +586,12 @@ hc_status_t hc_device_status(int clear) {
     const hc_status_t st = cuda_status(read_device_error(clear != 0, &v));
     if (st != HC_OK) return st;
     return v ? (hc_status_t)v : HC_OK;
+}
+
+hc_status_t hc_test_expire_waits(int enable) {
+    if (enable != 0 && enable != 1) return HC_ERR_INVALID_ARG;
+    set_test_expire_waits(enable == 1);
+    return HC_OK;
 }
 
 const char* hc_last_cuda_error(void) {

@@ -22,9 +22,10 @@ struct FusedParams {
     int p_intra;
     int pp;                    // RHD: power-of-two core size
     int rfold;                 // RHD: number of folded pairs
-    int stages;                // TMA kernels: pipeline depth
+    int hold;                  // TMA kernels: 1 = the wait-expiry test mode (see hc_test_expire_waits)
     int owner;                 // Broadcast: the root owns the single segment (-1: segment k's owner is k)
     unsigned long long skip_mask;  // AllGather / Broadcast: ranks whose data is already in place
+    unsigned long long wait_ns;    // TMA kernels: limit of the first wait on the copies' mbarrier
     int* err;                  // device address of the library's error flag (HC_ERR_TIMEOUT on a wait that gave up)
 };
 
@@ -140,7 +141,11 @@ __device__ __forceinline__ void st_stream(uintptr_t p, const uint4& v) { __stcs(
 // ---------------------------------------------------------------------------
 // bulk copies (cp.async.bulk) and mbarriers with bounded waits
 // ---------------------------------------------------------------------------
+// Limit of every wait on an mbarrier: a copy that has not landed after this
+// long is reported (HC_ERR_TIMEOUT) instead of being waited for forever.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+// Limit of the first wait in the wait-expiry test mode (hc_test_expire_waits).
+constexpr unsigned long long kTestWaitLimitNs = 1000000ull;
 
 __device__ __forceinline__ unsigned smem_addr(const void* p) {
     return (unsigned)__cvta_generic_to_shared(p);
@@ -167,12 +172,26 @@ __device__ __forceinline__ unsigned long long global_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
-// Poll an mbarrier phase for at most kWaitLimitNs.
-__device__ bool mbar_wait_bounded(uint64_t* m, unsigned parity) {
+// Poll an mbarrier phase for at most limit_ns.
+__device__ bool mbar_wait_bounded(uint64_t* m, unsigned parity, unsigned long long limit_ns) {
     const unsigned long long t0 = global_ns();
     while (!mbar_try_wait(m, parity))
-        if (global_ns() - t0 > kWaitLimitNs) return false;
+        if (global_ns() - t0 > limit_ns) return false;
     return true;
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* m) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(m)) : "memory");
+}
+// After a first wait on the copies' mbarrier `full` has expired: record
+// HC_ERR_TIMEOUT, release the arrival the test mode held back (hold = 1, on
+// the thread that issued the copies), and wait again, bounded by
+// kWaitLimitNs, until the bulk copies into this block's shared memory have
+// landed, so the block never exits with a copy into its shared memory in
+// flight.  A second expiry (a copy stuck for seconds) ends the wait anyway.
+__device__ __noinline__ void mbar_expired(uint64_t* full, int* err, int hold, bool issuer) {
+    atomicExch(err, (int)HC_ERR_TIMEOUT);
+    if (hold && issuer) mbar_arrive(full);
+    mbar_wait_bounded(full, 0, kWaitLimitNs);
 }
 __device__ __forceinline__ void bulk_g2s(void* smem_dst, uintptr_t gsrc, unsigned bytes, uint64_t* m) {
     asm volatile(
@@ -185,6 +204,19 @@ __device__ __forceinline__ void bulk_s2g(uintptr_t gdst, const void* smem_src, u
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
                  "r"(smem_addr(smem_src)), "r"(bytes)
                  : "memory");
+}
+// The same store with an L2 eviction-priority policy (createpolicy).
+__device__ __forceinline__ void bulk_s2g_hint(uintptr_t gdst, const void* smem_src, unsigned bytes,
+                                              uint64_t policy) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group.L2::cache_hint [%0], [%1], %2, %3;" ::"l"(gdst),
+                 "r"(smem_addr(smem_src)), "r"(bytes), "l"(policy)
+                 : "memory");
+}
+// Policy: lines written through it are the first evicted from L2.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -417,8 +449,13 @@ fused_reduce(const __grid_constant__ FusedParams p) {
 // mbarrier; then each thread reduces its 16-byte vector from shared memory
 // in the schedule's order and stores it to every output (AllReduce) or to the
 // owner's (ReduceScatter).  Shared memory: P tiles, so P <= kTmaMaxRanks.
-// The mbarrier wait is bounded: on expiry the block records HC_ERR_TIMEOUT in
-// *p.err, waits (again bounded) for its copies in flight and returns.
+// The mbarrier wait is bounded (p.wait_ns): on expiry the thread records
+// HC_ERR_TIMEOUT in *p.err, waits (bounded) for the block's copies in flight
+// and returns without storing (the call's outputs are then undefined).  In
+// the wait-expiry test mode (p.hold = 1) the mbarrier expects one arrival
+// more than the block makes before that first wait, so the first wait
+// expires although every copy lands; the copies' issuer makes the held
+// arrival once its own wait has expired.
 constexpr int kTmaThreads = 128;
 constexpr int kTmaTile = kTmaThreads * 16;  // bytes per rank per block
 constexpr int kTmaMaxRanks = 32;            // 64 KB of tiles per block
@@ -444,15 +481,14 @@ fused_reduce_tma(const __grid_constant__ FusedParams p) {
         const uintptr_t off = (uintptr_t)sbeg * ES + (uintptr_t)t0;
         uint64_t* full = (uint64_t*)(smem + (size_t)p.P * kTmaTile);
         if (threadIdx.x == 0) {
-            mbar_init(full, 1);
+            mbar_init(full, 1 + p.hold);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
             mbar_arrive_expect_tx(full, tb * (unsigned)p.P);
             for (int r = 0; r < p.P; r++) bulk_g2s(smem + (size_t)r * kTmaTile, p.src[r] + off, tb, full);
         }
         __syncthreads();  // the mbarrier is initialised before anyone polls it
-        if (!mbar_wait_bounded(full, 0)) {
-            atomicExch(p.err, (int)HC_ERR_TIMEOUT);
-            mbar_wait_bounded(full, 0);  // the copies in flight must land before the block exits
+        if (!mbar_wait_bounded(full, 0, p.wait_ns)) {
+            mbar_expired(full, p.err, p.hold, threadIdx.x == 0);
             return;
         }
         const unsigned vo = threadIdx.x * 16u;

@@ -133,6 +133,7 @@ hc_status_t hc_graph_build(hc_graph_t g) {
 hc_status_t hc_graph_launch(hc_graph_t g, hc_stream_t stream) {
     if (!g) return HC_ERR_INVALID_ARG;
     if (!g->exec) return HC_ERR_INVALID_ARG;  // not built
+    const hc::TraceRange range("hc_graph_launch", 0, (uint64_t)g->nodes.size());
     return cudaGraphLaunch(g->exec, (cudaStream_t)stream) == cudaSuccess ? HC_OK : HC_ERR_CUDA;
 }
 

@@ -14,6 +14,10 @@
 namespace hc {
 
 constexpr int kMaxRanks = HC_MAX_RANKS;
+// Devices the per-device host caches (SM counts, device addresses of the
+// library's __device__ variables) have room for; a higher ordinal is refused
+// with HC_ERR_CUDA.
+constexpr int kMaxDevices = 64;
 constexpr int kVecBytes = 16;  // one vector = 16 bytes = 4 x 32-bit or 8 x bf16
 
 // Buffer locations a step item can name, per rank.
@@ -81,6 +85,10 @@ struct StepParams {
     int64_t n;        // elements per rank vector
     int64_t lo, hi;   // slice of every segment for this launch (relative to the segment start)
     int64_t vecs;     // vectors per segment slice: ceil((hi - lo) / A)
+    int64_t tiles;    // TMA-staged step kernel: tiles of its tile size per segment slice
+    unsigned long long wait_ns;  // TMA-staged step kernel: limit of the first mbarrier wait
+    int* err;         // TMA-staged step kernel: device error flag (HC_ERR_TIMEOUT)
+    int32_t hold;     // TMA-staged step kernel: wait-expiry test mode
     int32_t nitems;
     int32_t total_ctas;
     DevItem items[MAXI];
@@ -179,12 +187,33 @@ hc_status_t execute(const Prepared& c, cudaStream_t stream);
 // true when b must wait for a (a write of one overlaps a read or write of the other)
 bool conflicts(const Prepared& a, const Prepared& b);
 
+// ---------------------------------------------------------------------------
+// Tracing (hc_trace.cpp): NVTX ranges in the "libhc" domain and HC_LOG lines.
+// ---------------------------------------------------------------------------
+uint32_t trace_category(hc_algo_t algo, hc_mode_t mode);
+class TraceRange {  // pushes a range on construction, pops it on destruction
+  public:
+    TraceRange(hc_coll_t coll, uint32_t category, uint64_t payload);
+    TraceRange(const char* msg, uint32_t category, uint64_t payload);
+    ~TraceRange();
+    TraceRange(const TraceRange&) = delete;
+    TraceRange& operator=(const TraceRange&) = delete;
+};
+bool log_enabled();  // HC_LOG is a nonzero integer (read once)
+void log_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int64_t n, hc_dtype_t dt,
+              int64_t loop_bytes, const Plan& plan);
+void log_fused(const Prepared& c);
+
 // Kernel launchers (hc_kernels.cu).
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count);
 // Reads (and optionally clears) the device-side error flag of the TMA kernels.
 cudaError_t read_device_error(bool clear, int* status);
+// Switches the wait-expiry test mode of the TMA-staged kernels (hc_test_expire_waits).
+void set_test_expire_waits(bool on);
+// host_buffers: some buffers are page-locked host memory (plain loads and
+// stores only, no bulk copies)
 cudaError_t launch_step(const Plan& plan, int P, hc_dtype_t dt, hc_op_t op,
                         const uintptr_t (&base)[LOC_COUNT][kMaxRanks], cudaStream_t stream,
-                        int sm_count);
+                        int sm_count, bool host_buffers);
 
 }  // namespace hc

@@ -33,6 +33,11 @@
 #include "hc_device.cuh"
 
 namespace hc {
+
+// Wait-expiry test mode (hc_test_expire_waits): read at each launch of a
+// TMA-staged kernel.
+std::atomic<int> g_test_expire_waits{0};
+
 namespace {
 
 // ---------------------------------------------------------------------------
@@ -158,6 +163,100 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
     }
 }
 
+// Step kernel, TMA-staged: for launches whose items combine three or more
+// operands (the intra-server mesh reduce of the Pipeline and of the
+// hierarchical AllReduce: up to p_intra inputs plus the partial that arrived
+// on the inter-server ring).  Block (item, segment, tile) bulk-copies tile
+// `tile` (kTmaTile bytes) of the launch's slice of that segment from every
+// operand -- the item's inputs in their order, then its accumulator -- into
+// consecutive kTmaTile slots of shared memory, all completing on one
+// mbarrier.  Each thread then combines its 16-byte vector exactly as
+// step_kernel does (in[0] (+) in[1] (+) ..., then acc (+) that) and stores it
+// to every output.  The mbarrier waits are bounded like fused_reduce_tma's.
+// On GB300 the register path (BATCH = 8, 4 blocks per SM) ran these
+// launches at 0.79 of the copy bandwidth.
+constexpr int kStepTmaMaxOperands = kTmaMaxRanks;  // shared memory <= 64 KB per block
+
+template <hc_dtype_t DT, hc_op_t OP, int MAXI>
+__global__ void __launch_bounds__(kTmaThreads)
+step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
+    constexpr int ES = DT_<DT>::ES;
+    constexpr int A = DT_<DT>::A;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int b = blockIdx.x;
+    int it = 0;
+    while (it + 1 < p.nitems && p.items[it + 1].cta_begin <= b) it++;
+    const DevItem& I = p.items[it];
+    const int64_t local = b - I.cta_begin;
+    const int si = (int)(local / p.tiles);
+    const int64_t tile = local - (int64_t)si * p.tiles;
+    const int seg = I.seg_first + (si / I.seg_width) * I.seg_stride + (si % I.seg_width);
+    const int64_t sbeg = (int64_t)seg * p.L;
+    const int64_t send_ = sbeg + p.L < p.n ? sbeg + p.L : p.n;
+    const int64_t hi = sbeg + p.hi < send_ ? sbeg + p.hi : send_;
+    const int64_t lo = sbeg + p.lo;
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (lo >= hi) return;  // the slice misses this (short) segment
+    const int64_t nfull = (hi - lo) / A;
+    const int64_t t0 = tile * kTmaTile;
+    const int acc_slot = I.acc_rank >= 0 ? I.in_cnt : -1;
+    const int nops = I.in_cnt + (acc_slot >= 0 ? 1 : 0);
+    if (t0 < nfull * 16) {
+        const int64_t left = nfull * 16 - t0;
+        const unsigned tb = (unsigned)(left < kTmaTile ? left : kTmaTile);
+        const uintptr_t off = (uintptr_t)lo * ES + (uintptr_t)t0;
+        uint64_t* full = (uint64_t*)(smem + (size_t)nops * kTmaTile);
+        if (threadIdx.x == 0) {
+            mbar_init(full, 1 + p.hold);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            mbar_arrive_expect_tx(full, tb * (unsigned)nops);
+            int r = I.in_rot;
+            for (int j = 0; j < I.in_cnt; j++) {
+                bulk_g2s(smem + (size_t)j * kTmaTile, p.base[I.in_loc][I.in_base + r] + off, tb, full);
+                if (++r == I.in_mod) r = 0;
+            }
+            if (acc_slot >= 0)
+                bulk_g2s(smem + (size_t)acc_slot * kTmaTile, p.base[I.acc_loc][I.acc_rank] + off, tb, full);
+        }
+        __syncthreads();  // the mbarrier is initialised before anyone polls it
+        if (!mbar_wait_bounded(full, 0, p.wait_ns)) {
+            mbar_expired(full, p.err, p.hold, threadIdx.x == 0);
+            return;
+        }
+        const unsigned vo = threadIdx.x * 16u;
+        if (vo < tb) {
+            uint4 v = *(const uint4*)(smem + vo);
+            for (int j = 1; j < I.in_cnt; j++)
+                v = vop<DT, OP>(v, *(const uint4*)(smem + (size_t)j * kTmaTile + vo));
+            if (acc_slot >= 0) v = vop<DT, OP>(*(const uint4*)(smem + (size_t)acc_slot * kTmaTile + vo), v);
+            int o = I.out_rot;
+            for (int j = 0; j < I.out_cnt; j++) {
+                st_vec(p.base[I.out_loc][I.out_base + o] + off + vo, v);
+                if (++o == I.out_mod) o = 0;
+            }
+        }
+    }
+    if (tile == 0 && threadIdx.x == 0) {
+        // ragged end of the rank vector (< 16 bytes): element by element
+        for (int64_t x = lo + nfull * A; x < hi; x++) {
+            const uintptr_t xo = (uintptr_t)x * ES;
+            int rr = I.in_rot;
+            uint32_t v = ld_elem<ES>(p.base[I.in_loc][I.in_base + rr] + xo);
+            for (int j = 1; j < I.in_cnt; j++) {
+                if (++rr == I.in_mod) rr = 0;
+                v = vop<DT, OP>(v, ld_elem<ES>(p.base[I.in_loc][I.in_base + rr] + xo));
+            }
+            if (acc_slot >= 0) v = vop<DT, OP>(ld_elem<ES>(p.base[I.acc_loc][I.acc_rank] + xo), v);
+            int o = I.out_rot;
+            for (int j = 0; j < I.out_cnt; j++) {
+                st_elem<ES>(p.base[I.out_loc][I.out_base + o] + xo, v);
+                if (++o == I.out_mod) o = 0;
+            }
+        }
+    }
+}
+
 // AllGather, register path: segment k read once from its owner, written to
 // every rank (the owner's own copy only when it is not already in place).
 // Broadcast is the same kernel with one segment owned by the root.
@@ -196,8 +295,10 @@ fused_allgather(const __grid_constant__ FusedParams p) {
 // between HBM and shared memory with the bulk-copy engine (cp.async.bulk),
 // completion tracked by an mbarrier transaction count, and bulk-stores it from
 // shared memory to all outputs.  Every wait on the mbarrier is bounded: after
-// kWaitLimitNs the block records HC_ERR_TIMEOUT in hc_device_error, waits
-// (again bounded) for its copy in flight and returns.
+// p.wait_ns the block records HC_ERR_TIMEOUT in hc_device_error, waits
+// (again bounded) for its copy in flight and returns without storing; in the
+// wait-expiry test mode (p.hold) the first wait expires by construction, as
+// in fused_reduce_tma.
 // ---------------------------------------------------------------------------
 // One 32 KB tile per block, a block for every tile of every segment: blocks
 // are scheduled in index order, so the stores sweep each output from its
@@ -232,17 +333,19 @@ fused_allgather_tma(const __grid_constant__ FusedParams p) {
         const int64_t left = nbytes - t0;
         const unsigned tb = (unsigned)(left < kAgTile ? left : kAgTile);
         const uintptr_t off = (uintptr_t)sbeg * ES + (uintptr_t)t0;
-        mbar_init(full, 1);
+        mbar_init(full, 1 + p.hold);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         mbar_arrive_expect_tx(full, tb);
         bulk_g2s(smem, p.src[k] + off, tb, full);
-        if (!mbar_wait_bounded(full, 0)) {
-            atomicExch(&hc_device_error, (int)HC_ERR_TIMEOUT);
-            mbar_wait_bounded(full, 0);  // the copy in flight must land before the block exits
+        if (!mbar_wait_bounded(full, 0, p.wait_ns)) {
+            mbar_expired(full, p.err, p.hold, true);
             return;
         }
+        // each output line is written once and not read again here: let
+        // it leave L2 first (on GB300, P = 32: 156 against 160 us)
+        const uint64_t pol = l2_evict_first_policy();
         for (int r = 0; r < p.P; r++)
-            if (r != k || !skip_own) bulk_s2g(p.dst[r] + off, smem, tb);
+            if (r != k || !skip_own) bulk_s2g_hint(p.dst[r] + off, smem, tb, pol);
         bulk_commit();
         bulk_wait_all();
     }
@@ -283,9 +386,9 @@ void* pick_reduce_tma(hc_algo_t algo, int coll, hc_dtype_t dt, hc_op_t op, int P
 // Device address of hc_device_error on the current device (looked up once
 // per device).
 int* device_error_flag() {
-    static std::atomic<int*> addr[64];  // null-initialised (static storage)
+    static std::atomic<int*> addr[kMaxDevices];  // null-initialised (static storage)
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
     int* a = addr[dev].load(std::memory_order_acquire);
     if (!a) {
         void* p = nullptr;
@@ -350,6 +453,24 @@ void* pick_step_op(hc_op_t op) {
     default: return (void*)step_kernel<DT, HC_MIN, MAXI, BATCH>;
     }
 }
+template <int MAXI, hc_dtype_t DT>
+void* pick_step_tma_op(hc_op_t op) {
+    switch (op) {
+    case HC_SUM: return (void*)step_kernel_tma<DT, HC_SUM, MAXI>;
+    case HC_PROD: return (void*)step_kernel_tma<DT, HC_PROD, MAXI>;
+    case HC_MAX: return (void*)step_kernel_tma<DT, HC_MAX, MAXI>;
+    default: return (void*)step_kernel_tma<DT, HC_MIN, MAXI>;
+    }
+}
+template <int MAXI>
+void* pick_step_tma(hc_dtype_t dt, hc_op_t op) {
+    switch (dt) {
+    case HC_INT32: return pick_step_tma_op<MAXI, HC_INT32>(op);
+    case HC_FLOAT32: return pick_step_tma_op<MAXI, HC_FLOAT32>(op);
+    default: return pick_step_tma_op<MAXI, HC_BFLOAT16>(op);
+    }
+}
+
 template <int MAXI, int BATCH>
 void* pick_step(hc_dtype_t dt, hc_op_t op) {
     switch (dt) {
@@ -384,7 +505,7 @@ template <int MAXI>
 cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t first, size_t count,
                               hc_dtype_t dt, hc_op_t op,
                               const uintptr_t (&base)[LOC_COUNT][kMaxRanks],
-                              cudaStream_t stream, int sm_count) {
+                              cudaStream_t stream, int sm_count, bool host_buffers) {
     static thread_local StepParams<MAXI> p;  // large: keep it off the stack
     std::memcpy(p.base, base, sizeof(p.base));
     p.L = plan.lay.L;
@@ -392,16 +513,42 @@ cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t firs
     p.lo = L.lo;
     p.hi = L.hi;
     p.vecs = (L.hi - L.lo + plan.lay.A - 1) / plan.lay.A;
+    p.tiles = 0;
+    p.hold = g_test_expire_waits.load() ? 1 : 0;
+    p.wait_ns = p.hold ? kTestWaitLimitNs : kWaitLimitNs;
+    p.err = nullptr;
     PlanLaunch part;
     part.lo = L.lo;
     part.hi = L.hi;
     part.items.assign(L.items.begin() + first, L.items.begin() + first + count);
-    int widest = 1;
-    for (const DevItem& it : part.items) widest = std::max(widest, (int)it.in_cnt);
+    int widest = 1, operands = 1;
+    for (const DevItem& it : part.items) {
+        widest = std::max(widest, (int)it.in_cnt);
+        operands = std::max(operands, it.in_cnt + (it.acc_rank >= 0 ? 1 : 0));
+    }
+    p.nitems = (int)count;
+    if (widest >= 3 && operands <= kStepTmaMaxOperands && !host_buffers) {
+        // TMA-staged: one block per tile of every segment of every item
+        void* fn = pick_step_tma<MAXI>(dt, op);
+        p.err = device_error_flag();
+        if (!p.err) return cudaErrorInvalidValue;
+        const int smem = operands * kTmaTile + 16;
+        if (!allow_smem(fn, smem)) return cudaErrorInvalidValue;
+        p.tiles = std::max<int64_t>(1, (p.vecs * 16 + kTmaTile - 1) / kTmaTile);
+        int64_t begin = 0;
+        for (DevItem& it : part.items) {
+            it.cta_begin = (int32_t)begin;
+            begin += (int64_t)it.seg_width * it.seg_reps * p.tiles;
+        }
+        if (begin > INT32_MAX) return cudaErrorInvalidValue;
+        p.total_ctas = (int)begin;
+        std::memcpy(p.items, part.items.data(), count * sizeof(DevItem));
+        void* args[] = {&p};
+        return launch_pdl(fn, dim3((unsigned)begin), dim3(kTmaThreads), args, smem, stream);
+    }
     void* fn = widest >= 3 ? pick_step<MAXI, kStepBatch>(dt, op) : pick_step<MAXI, 1>(dt, op);
     // one wave of resident blocks
     const int grid = assign_ctas(part, plan.lay, kStepThreads, sm_count * resident_blocks(fn));
-    p.nitems = (int)count;
     p.total_ctas = grid;
     std::memcpy(p.items, part.items.data(), count * sizeof(DevItem));
     void* args[] = {&p};
@@ -412,23 +559,28 @@ cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t firs
 
 cudaError_t launch_step(const Plan& plan, int P, hc_dtype_t dt, hc_op_t op,
                         const uintptr_t (&base)[LOC_COUNT][kMaxRanks], cudaStream_t stream,
-                        int sm_count) {
+                        int sm_count, bool host_buffers) {
     (void)P;
+    uint64_t index = 0;
     for (const PlanLaunch& L : plan.launches) {
+        const TraceRange range("hc step launch", 0, index++);
         size_t ni = L.items.size();
         cudaError_t e = cudaSuccess;
         if (ni <= (size_t)kSmallItems) {
-            e = launch_step_items<kSmallItems>(plan, L, 0, ni, dt, op, base, stream, sm_count);
+            e = launch_step_items<kSmallItems>(plan, L, 0, ni, dt, op, base, stream, sm_count,
+                                               host_buffers);
         } else {
             // items of one step are independent, so a step may be split
             for (size_t f = 0; f < ni && e == cudaSuccess; f += kLargeItems)
                 e = launch_step_items<kLargeItems>(plan, L, f, std::min(ni - f, (size_t)kLargeItems),
-                                                   dt, op, base, stream, sm_count);
+                                                   dt, op, base, stream, sm_count, host_buffers);
         }
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
 }
+
+void set_test_expire_waits(bool on) { g_test_expire_waits.store(on ? 1 : 0); }
 
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) {
     FusedParams p;
@@ -436,6 +588,8 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     const int es = elem_bytes(a.dtype);
     const Layout& lay = a.lay;
     p.owner = -1;
+    p.hold = g_test_expire_waits.load() ? 1 : 0;
+    p.wait_ns = p.hold ? kTestWaitLimitNs : kWaitLimitNs;
     for (int r = 0; r < a.P; r++) {
         if (a.coll == HC_COLL_BROADCAST) {
             // the root's input is the whole vector (segment 0 starts at 0)
@@ -481,10 +635,18 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     // 6.3 TB/s.  Buffers in page-locked host memory keep a persistent grid
     // (the host link, not HBM, bounds them).
     if (a.coll == HC_COLL_ALLGATHER || a.coll == HC_COLL_BROADCAST) {
-        // TMA path once every segment holds several tiles; buffers in host
-        // memory take the plain load / store path
-        if (seg_bytes >= 16 * (int64_t)kAgTile && !a.host_buffers) {
+        // TMA path for 16 or more ranks once every segment holds several
+        // tiles; fewer ranks, and buffers in host memory, take the plain
+        // load / store path.  On GB300 (fp32, out of place, same call): P = 8,
+        // 64 MiB per rank: register path 92.3 - 93.5 us, TMA 95.0 - 96.5 us;
+        // P = 32, 32 MiB per rank: register path 166 us, TMA with
+        // evict-first stores 156 us.  The same store pattern without the
+        // loads takes 73.8 us (P = 8), so the 64 MiB of reads cost about
+        // 19 us of a 92 us call: reads and writes share the DRAM bus.
+        if (a.P >= 16 && seg_bytes >= 16 * (int64_t)kAgTile && !a.host_buffers) {
             void* fn = es == 2 ? (void*)fused_allgather_tma<2> : (void*)fused_allgather_tma<4>;
+            p.err = device_error_flag();
+            if (!p.err) return cudaErrorInvalidValue;
             const int smem = kAgTile + 16;
             if (!allow_smem(fn, smem)) return cudaErrorInvalidValue;
             const int64_t tiles = (seg_bytes + kAgTile - 1) / kAgTile;

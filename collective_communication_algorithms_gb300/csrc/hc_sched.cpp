@@ -690,20 +690,30 @@ static int64_t item_vectors(const DevItem& it, const PlanLaunch& L, const Layout
     return v * (int64_t)it.seg_width * it.seg_reps;
 }
 
+// CTAs per item: one per `threads` vectors when the budget allows; otherwise
+// the budget is shared in proportion to the bytes each item moves (vectors x
+// its inputs, accumulator and outputs), so that items of one launch finish
+// together.  (Shared by vectors alone, a Pipeline AllGather step whose 1 -> 7
+// broadcast items sit beside 1 -> 1 forwards gave both kinds the same CTAs
+// and ran at 0.68 of the copy bandwidth on GB300.)
 int assign_ctas(PlanLaunch& L, const Layout& lay, int threads, int max_ctas) {
     const int ni = (int)L.items.size();
     if (ni == 0) return 0;
-    std::vector<int64_t> need(ni);
-    int64_t total = 0;
+    std::vector<int64_t> need(ni), weight(ni);
+    int64_t total = 0, wsum = 0;
     for (int i = 0; i < ni; i++) {
-        need[i] = std::max<int64_t>(1, cdiv(item_vectors(L.items[i], L, lay), threads));
+        const DevItem& it = L.items[i];
+        const int64_t v = item_vectors(it, L, lay);
+        need[i] = std::max<int64_t>(1, cdiv(v, threads));
+        weight[i] = std::max<int64_t>(1, v) * (it.in_cnt + (it.acc_rank >= 0 ? 1 : 0) + it.out_cnt);
         total += need[i];
+        wsum += weight[i];
     }
-    int budget = std::max(max_ctas, ni);
+    const int budget = std::max(max_ctas, ni);
     int begin = 0;
     for (int i = 0; i < ni; i++) {
         int64_t c = need[i];
-        if (total > budget) c = std::max<int64_t>(1, need[i] * budget / total);
+        if (total > budget) c = std::min(need[i], std::max<int64_t>(1, weight[i] * budget / wsum));
         L.items[i].cta_begin = begin;
         begin += (int)c;
     }

@@ -234,12 +234,22 @@ hc_status_t hc_broadcast(const void* send, void* const* recv, int P, size_t coun
  * HC_STATIC_SCRATCH_BYTES that the library places in the memory of every GPU
  * that loads it, held until the process exits.  It calls no cudaMalloc,
  * cudaFree or other allocating routine.
- *  - Work needing more than HC_STATIC_SCRATCH_BYTES (P * roundup(count * b,
- *    256) bytes, see hc_scratch_bytes) is rejected with HC_ERR_SCRATCH before
- *    anything is launched.
- *  - The first call on a device, with that device current, looks up the
- *    array's device address (cudaGetSymbolAddress); make that first call
- *    before any stream capture.
+ *  - Every argument is validated first, exactly as hc_reduce_scatter does,
+ *    before the device is touched.  Work needing more than
+ *    HC_STATIC_SCRATCH_BYTES (P * roundup(count * b, 256) bytes, see
+ *    hc_scratch_bytes) is then rejected with HC_ERR_SCRATCH; nothing is
+ *    launched.  A call whose ranks are all in place needs no scratch and
+ *    never touches the array.
+ *  - The first call on a device that needs the scratch, with that device
+ *    current, looks up the array's device address (cudaGetSymbolAddress);
+ *    make that first call before any stream capture.  Under lazy module
+ *    loading (CUDA_MODULE_LOADING=LAZY, the runtime's default) the array is
+ *    committed inside that lookup, so the first call can fail with
+ *    HC_ERR_CUDA when the device cannot give it HC_STATIC_SCRATCH_BYTES at
+ *    that moment; set CUDA_MODULE_LOADING=EAGER to commit it when the
+ *    runtime initialises the device instead.  The address is looked up once
+ *    per device ordinal: do not keep using the library across a
+ *    cudaDeviceReset() of that device.
  *  - All calls share the one array and it keeps whatever the last call left
  *    there; nothing in it needs to start at zero, because every location is
  *    written before it is read within a call.  Calls that overlap on the GPU
@@ -404,8 +414,26 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
  * Returns HC_OK, HC_ERR_TIMEOUT, or HC_ERR_CUDA if the flag cannot be read.
  * Synchronises with the current device (it copies the flag to the host);
  * clear != 0 resets the flag.
+ * A block whose wait gave up waits once more, also bounded, for the copies
+ * into its own shared memory to land, and then exits without storing: the
+ * outputs of the call that reported HC_ERR_TIMEOUT are undefined, and later
+ * calls are unaffected.
  */
 hc_status_t hc_device_status(int clear);
+
+/*
+ * Test hook for the path above (no counterpart on the pages).  enable = 1
+ * switches every TMA-staged fused kernel launched from then on (any host
+ * thread) into a mode in which the copies' shared-memory barrier waits for
+ * one arrival more than the block makes before its first wait, and that
+ * first wait gives up after 1 ms instead of 2 s.  Every copy still lands;
+ * the first wait expires regardless, the block records HC_ERR_TIMEOUT, makes
+ * the held arrival, waits (bounded) for its copies and exits without
+ * storing.  Nothing hangs or faults.  enable = 0 restores normal operation.
+ * Returns HC_ERR_INVALID_ARG for any other value.  Not for production use:
+ * calls launched in this mode leave their outputs undefined.
+ */
+hc_status_t hc_test_expire_waits(int enable);
 
 /* Name of the CUDA error (e.g. "cudaErrorInvalidValue") behind the last
  * HC_ERR_CUDA this host thread received; "cudaSuccess" if none. */

@@ -310,13 +310,14 @@ def test_fused_around_the_tma_rank_limit(algo, dtype):
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_tma_staged_paths(algo, dtype):
-    """Segments long enough for the TMA-staged AllGather (at least 16 tiles of
-    32 KB per segment), with a partial last tile and a ragged end; AllReduce and
-    ReduceScatter at the same sizes (register path with every launch shape the
-    library picks: 4- and 2-byte types, sum and max)."""
+    """Segments long enough for the TMA-staged AllGather (16 or more ranks and
+    at least 16 tiles of 32 KB per segment; fewer ranks take the register
+    path), with a partial last tile and a ragged end; AllReduce and
+    ReduceScatter at the same sizes (TMA-staged reduce, and the register path
+    where the library picks it: 4- and 2-byte types, sum and max)."""
     from collective_communication_algorithms_gb300 import _binding as B
     per_seg = 70000 if dtype != "bfloat16" else 135000
-    for P in (2, 3, 5, 8):
+    for P in (2, 3, 5, 8, 16, 17):
         pin = intra_for(algo, P) if algo != "pipeline" else (2 if P % 2 == 0 else 1)
         n = P * per_seg + 13
         for op in ("sum", "max"):

@@ -619,3 +619,56 @@ def test_plan_cache_under_concurrent_host_threads():
         th.join(timeout=300)
     assert not errors, errors
     assert all(not th.is_alive() for th in threads)
+
+
+def test_wait_expiry_switch_accepts_only_zero_or_one():
+    """hc_test_expire_waits takes 0 or 1 (host only: it sets a flag read at
+    the next launch of a TMA-staged kernel)."""
+    assert B.lib().hc_test_expire_waits(2) == 1  # HC_ERR_INVALID_ARG
+    assert B.lib().hc_test_expire_waits(-1) == 1
+    assert B.lib().hc_test_expire_waits(0) == 0
+
+
+HC_LOG_PROGRAM = r"""
+import sys
+sys.path.insert(0, %r)
+from collective_communication_algorithms_gb300 import _binding as B
+P, n = 32, 8388608
+send = [(1 << 40) + r * (64 << 20) for r in range(P)]
+recv = [(1 << 41) + r * (64 << 20) for r in range(P)]
+opts = B.make_opts("step", ranks_per_server=8, max_loop_bytes=64 << 20)
+for _ in range(2):  # the plan is built (and logged) once, then taken from the cache
+    try:
+        B.hc_allreduce(send, recv, P, n, "float32", "sum", "pipeline", opts, 0)
+    except B.HcError as e:
+        print("status", e.status)
+"""
+
+
+@host_only
+def test_hc_log_reports_the_pipeline_loops():
+    """HC_LOG=1 prints one line per step-mode plan the library builds: for the
+    4 x 8 Pipeline AllReduce of 8,388,608 fp32 elements per rank with a
+    64 MiB loop limit it names the schedule, 8 steps per loop, 4 loops of
+    74,880 elements per segment, the 37,504-element tail and 32 launches
+    (the Pipeline article logs its loop count before running the loops).
+    The plan is built before any launch, so no GPU is needed; the call
+    itself then fails for want of a device."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, HC_LOG="1")
+    out = subprocess.run([sys.executable, "-c", HC_LOG_PROGRAM % root], env=env,
+                         capture_output=True, text=True, timeout=120)
+    lines = [ln for ln in out.stderr.splitlines() if ln.startswith("hc: plan ")]
+    assert len(lines) == 1, out.stderr
+    line = lines[0]
+    for field in ("allreduce pipeline", "P=32", "ranks_per_server=8", "n=8388608", "float32",
+                  "max_loop_bytes=67108864", "steps_per_loop=8", "loops=4", "chunk=74880",
+                  "tail=37504", "launches=32"):
+        assert field in line, (field, line)
+    assert out.stdout.count("status 5") == 2  # HC_ERR_CUDA: no device
+    env.pop("HC_LOG")
+    quiet = subprocess.run([sys.executable, "-c", HC_LOG_PROGRAM % root], env=env,
+                           capture_output=True, text=True, timeout=120)
+    assert "hc: " not in quiet.stderr

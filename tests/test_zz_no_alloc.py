@@ -4,7 +4,9 @@ hands only input and output buffers, or a latency-critical path that cannot
 afford cudaMalloc).  Its working memory is a fixed array inside the library,
 so these tests check that it gives exactly what the ordinary entry point
 gives with caller-provided scratch, on two calls in a row (the array keeps the
-first call's contents), and that work too large for the array is refused.
+first call's contents), that it matches the oracle's replay directly, that a
+call after the first on a device changes the device's free memory by not one
+byte, and that work too large for the array is refused.
 
 The file is named so that pytest collects it last.
 """
@@ -12,6 +14,7 @@ import numpy as np
 import pytest
 
 import hc_inputs
+import oracle as O
 
 pytestmark = pytest.mark.gpu
 torch = pytest.importorskip("torch")
@@ -79,6 +82,35 @@ def test_matches_existing_entry_point_on_two_calls_in_a_row():
     _reduce_scatter_both_ways("rhd", X3)
     X4 = hc_inputs.gradients_f32(32, 50001, seed=24)
     _reduce_scatter_both_ways("pipeline", X4, ranks_per_server=8, loop_bytes=1 << 20)
+
+
+def test_allocates_nothing_and_matches_the_oracle():
+    """After a first call on the device (which, under lazy module loading,
+    is where the array is committed), a second call leaves the device's free
+    memory unchanged, and both calls' outputs equal the oracle's replay of
+    the Ring ReduceScatter bit for bit."""
+    P, n = 8, 300001
+    X = hc_inputs.gradients_f32(P, n, seed=31)
+    Y = O.replay("ring", "reducescatter", X, "sum", "float32")
+    src = _rank_buffers(X)
+    sp = [src[r].data_ptr() for r in range(P)]
+    segs, outs = _outputs("ring", P, n)
+    op = [t.data_ptr() for t in outs]
+    stream = torch.cuda.current_stream().cuda_stream
+    free = []
+    for _ in range(2):
+        torch.cuda.synchronize()
+        free.append(torch.cuda.mem_get_info()[0])
+        B.hc_reduce_scatter_static_scratch(sp, op, P, n, "float32", "sum", "ring", 1, 0, stream)
+        torch.cuda.synchronize()
+        for r, (off, ln) in enumerate(segs):
+            got = outs[r][:ln].cpu().numpy().view(np.uint32)
+            assert np.array_equal(got, Y[r, off:off + ln].view(np.uint32)), r
+        for t in outs:
+            t.fill_(float("nan"))
+    torch.cuda.synchronize()
+    free.append(torch.cuda.mem_get_info()[0])
+    assert free[1] == free[2], "the second call changed the device's free memory"
 
 
 def test_rejects_work_larger_than_the_array():
