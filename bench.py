@@ -85,6 +85,47 @@ WORKLOADS = {
                                    algo="rhd", coll="allreduce", P=8, n=4096, dtype="float32",
                                    op="sum", mode="step", p_intra=1, loop_bytes=0, scale=1.0),
 }
+
+
+def _add(name, desc, algo, coll, P, n, dtype, op, mode, p_intra=1, loop_bytes=0, scale=1e-3):
+    WORKLOADS[name] = dict(desc=desc, algo=algo, coll=coll, P=P, n=n, dtype=dtype, op=op, mode=mode,
+                           p_intra=p_intra, loop_bytes=loop_bytes, scale=scale)
+
+
+# the rest of the benchmark's configurations, each a workload of its own
+_add("ring_fp32_p8_rs_step", "Ring ReduceScatter sum, P=8, fp32, 16,777,216 elements per rank, "
+     "step mode, out of place (caller scratch)", "ring", "reducescatter", 8, 16777216, "float32",
+     "sum", "step")
+_add("ring_fp32_p8_ag_step", "Ring AllGather, P=8, fp32, 16,777,216 elements per rank, step mode, "
+     "out of place", "ring", "allgather", 8, 16777216, "float32", "sum", "step")
+for _a in ("ring", "rhd"):
+    for _o in ("sum", "max"):
+        for _m in ("fused", "step"):
+            _k = "%s_bf16_p8%s%s" % (_a, "" if _o == "sum" else "_max", "" if _m == "fused" else "_step")
+            if _k not in WORKLOADS:
+                _add(_k, "%s AllReduce %s, P=8, bf16 (per-step rounding), 67,108,864 elements per "
+                     "rank (128 MiB), N(0,1)*1e-2, %s mode" % (_a.upper() if _a == "rhd" else "Ring",
+                                                               _o, _m),
+                     _a, "allreduce", 8, 67108864, "bfloat16", _o, _m, scale=1e-2)
+for _c, _t in (("reducescatter", "rs"), ("allgather", "ag")):
+    _add("pipe_fp32_4x8_%s" % _t, "Pipeline %s, 4 servers x 8 ranks (P=32), fp32, 8,388,608 "
+         "elements per rank, fused" % ("ReduceScatter" if _t == "rs" else "AllGather"),
+         "pipeline", _c, 32, 8388608, "float32", "sum", "fused", p_intra=8)
+    _add("pipe_fp32_4x8_%s_step" % _t, "Pipeline %s, 4x8, fp32, 8,388,608 elements per rank, step "
+         "mode, 64 MiB loop limit (4 loops, tail 37,504)" % ("ReduceScatter" if _t == "rs" else
+                                                             "AllGather"),
+         "pipeline", _c, 32, 8388608, "float32", "sum", "step", p_intra=8, loop_bytes=64 << 20)
+
+# The configurations timed in one default run (N = 1), grouped by their
+# input buffers (each group's rank vectors are drawn once).
+SWEEP = [
+    ["ring_fp32_p8_step", "ring_fp32_p8_rs", "ring_fp32_p8_rs_step", "ring_fp32_p8_ag",
+     "ring_fp32_p8_ag_step"],
+    ["ring_bf16_p8", "ring_bf16_p8_max", "rhd_bf16_p8", "rhd_bf16_p8_max", "ring_bf16_p8_step",
+     "ring_bf16_p8_max_step", "rhd_bf16_p8_step", "rhd_bf16_p8_max_step"],
+    ["pipe_fp32_4x8", "pipe_fp32_4x8_rs", "pipe_fp32_4x8_ag", "pipe_fp32_4x8_step",
+     "pipe_fp32_4x8_rs_step", "pipe_fp32_4x8_ag_step", "hier_fp32_4x8", "hier_fp32_4x8_step"],
+]
 DTYPE_TAG = {"float32": "f32", "bfloat16": "bf16", "int32": "int32"}
 ESIZE = {"float32": 4, "bfloat16": 2, "int32": 4}
 KERNEL_DIR = os.path.join(ROOT, "collective_communication_algorithms_gb300", "csrc")
@@ -101,6 +142,8 @@ def parse_args():
     ap.add_argument("--workload", default="ring_fp32_p8", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other configurations (the `configs` array of the line)")
     ap.add_argument("--sweep", choices=["small", "select", "hostlink", "hbm"], default=None,
                     help="small: RHD AllReduce latency sweep (P x n), eager vs graph mode; "
                          "select: cost-model selector against measured times; "
@@ -265,6 +308,212 @@ def replica_algbw(world, bytes_per_rank, ms):
 # ---------------------------------------------------------------------------
 # our implementation
 # ---------------------------------------------------------------------------
+class Collective:
+    """One workload's device buffers and its call through the C ABI.
+    send: the (P, n) rank vectors on the device (bf16 as int16 bits); the
+    outputs are new (P, n) rows (AllReduce, AllGather) or one buffer per
+    segment (ReduceScatter), all out of place; a step-mode ReduceScatter gets
+    the scratch hc_scratch_bytes asks for."""
+
+    def __init__(self, B, w, send, stream):
+        import torch
+        P, n, dt = w["P"], w["n"], w["dtype"]
+        self.B, self.w, self.stream = B, w, stream
+        self.send = send
+        self.recv = torch.empty_like(send)
+        send_p = [send[r].data_ptr() for r in range(P)]
+        recv_p = [self.recv[r].data_ptr() for r in range(P)]
+        self.segs = self.rs_out = self.ag_in = self.scratch = None
+        if w["coll"] in ("reducescatter", "allgather"):
+            self.segs = [B.hc_segment_range(w["algo"], w["coll"], P, n, dt, k) for k in range(P)]
+        if w["coll"] == "reducescatter":
+            self.rs_out = [torch.empty(max(ln, 8), dtype=send.dtype, device=send.device)
+                           for _, ln in self.segs]
+            recv_p = [t.data_ptr() for t in self.rs_out]
+        if w["coll"] == "allgather":
+            self.ag_in = [send[k, off:off + ln].clone() for k, (off, ln) in enumerate(self.segs)]
+            send_p = [t.data_ptr() for t in self.ag_in]
+        sb = 0
+        if w["coll"] == "reducescatter" and w["mode"] == "step":
+            sb = B.hc_scratch_bytes(w["algo"], P, n, dt)
+            self.scratch = torch.empty(sb, dtype=torch.uint8, device=send.device)
+        self.opts = B.make_opts(w["mode"], ranks_per_server=w["p_intra"],
+                                max_loop_bytes=w["loop_bytes"],
+                                scratch=self.scratch.data_ptr() if sb else 0, scratch_bytes=sb)
+        self.sp, self.rp = B.ptr_array(send_p), B.ptr_array(recv_p)
+
+    def __call__(self):
+        B, w = self.B, self.w
+        P, n, dt = w["P"], w["n"], w["dtype"]
+        if w["coll"] == "allreduce":
+            B.hc_allreduce(self.sp, self.rp, P, n, dt, w["op"], w["algo"], self.opts, self.stream)
+        elif w["coll"] == "reducescatter":
+            B.hc_reduce_scatter(self.sp, self.rp, P, n, dt, w["op"], w["algo"], self.opts,
+                                self.stream)
+        else:
+            B.hc_allgather(self.sp, self.rp, P, n, dt, w["algo"], self.opts, self.stream)
+
+
+def step_call_stats(B, w):
+    """(kernel launches, bytes the step kernels read + write) of one
+    out-of-place step-mode call of workload w, from its exported plan: every
+    record moves (hi - lo) elements of each input, the accumulator and each
+    output."""
+    recs, launches = B.hc_step_plan(w["algo"], w["coll"], w["P"], w["n"], w["dtype"], w["p_intra"],
+                                    w["loop_bytes"], in_place=False)
+    b = ESIZE[w["dtype"]]
+    moved = sum((r["hi"] - r["lo"]) * b * (len(r["in_ranks"]) + (r["acc_rank"] >= 0) +
+                                          len(r["out_ranks"])) for r in recs)
+    return launches, moved
+
+
+def time_device(call, steps, warmup, stream):
+    """W untimed calls, then K calls queued behind a spin kernel and timed
+    with CUDA events on the launch stream: (ms per call over the whole
+    region, mean ms between the events around each call)."""
+    import torch
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ka = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    hold_device(steps)
+    ev0.record(stream)
+    for i in range(steps):
+        ka[i].record(stream)
+        call()
+        kb[i].record(stream)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    return (ev0.elapsed_time(ev1) / steps,
+            statistics.mean(a.elapsed_time(bb) for a, bb in zip(ka, kb)))
+
+
+def time_queued(call, reps, stream):
+    """Device microseconds per call of `reps` calls queued behind a spin
+    kernel, with CUDA events only around the whole batch (events between
+    calls would break the launches' programmatic overlap and, for calls of a
+    few microseconds, dominate them)."""
+    import torch
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    hold_device(reps)
+    e0.record(stream)
+    for _ in range(reps):
+        call()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / reps * 1e3
+
+
+def config_sweep(args, dev):
+    """Every configuration of the benchmark besides the headline, timed like
+    it: the large ones (SWEEP) as algbw and fraction of the copy peak, the
+    latency regime (int32 P = 4 Ring and P = 5 RHD at 4096 elements; RHD fp32
+    P in {5, 8, 12, 16} x 256 .. 16384 elements) as microseconds per call."""
+    import torch
+    from collective_communication_algorithms_gb300 import _binding as B
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    peak, _ = measured_peak()
+    out = []
+    for group in SWEEP:
+        w0 = WORKLOADS[group[0]]
+        X = inputs_for(w0)
+        Xd = torch.from_numpy(X.view(np.int16) if w0["dtype"] == "bfloat16" else X).to(dev)
+        del X
+        for name in group:
+            w = WORKLOADS[name]
+            P, n, dt = w["P"], w["n"], w["dtype"]
+            c = Collective(B, w, Xd, sh)
+            if w["mode"] == "fused":
+                launches, alg = 1, algorithmic_bytes(w)
+            else:
+                launches, alg = step_call_stats(B, w)
+            ms, kern = time_device(c, args.steps, args.warmup, stream)
+            out.append({"name": name, "workload": w["desc"],
+                        "value": round(n * ESIZE[dt] / (ms * 1e-3) / 1e9, 3), "unit": "GB/s",
+                        "ms_per_call": round(ms, 5), "kernel_ms": round(kern, 5),
+                        "bytes_per_call": alg, "bytes": "fused minimum" if w["mode"] == "fused"
+                        else "step mode's own (inputs + accumulator + outputs of every step)",
+                        "achieved_GBps": round(alg / (kern * 1e-3) / 1e9, 1),
+                        "frac": round(alg / (kern * 1e-3) / 1e9 / peak, 4),
+                        "traffic": traffic_from_profiles(name), "launches_per_call": launches,
+                        "l2": l2_note(w["coll"], P, n * ESIZE[dt])})
+            del c
+        del Xd
+        torch.cuda.empty_cache()
+    out += latency_sweep(B, dev)
+    return out
+
+
+def latency_sweep(B, dev, reps=100):
+    """Per-call microseconds of small in-place AllReduces (hot L2): `eager`
+    is back-to-back calls from Python (host and device overlap, so the
+    slower of the two decides), `queued` the same calls enqueued behind a
+    spin kernel (the device's own time per call), `graph` one CUDA graph of
+    `reps` calls (graph mode) launched once."""
+    import math
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    points = [("int32_ring_p4", "ring", "int32", 4, 4096), ("int32_rhd_p5", "rhd", "int32", 5, 4096)]
+    points += [("rhd_fp32_small", "rhd", "float32", P, n)
+               for P in (5, 8, 12, 16) for n in (256, 512, 1024, 2048, 4096, 8192, 16384)]
+    out = []
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for name, algo, dt, P, n in points:
+        X = hc_inputs.uniform_int32(P, n, seed=0) if dt == "int32" else \
+            hc_inputs.gradients_f32(P, n, seed=0, scale=1.0)
+        xd = torch.from_numpy(X).to(dev)
+        ptrs = B.ptr_array([xd[r].data_ptr() for r in range(P)])
+        st, _ = B.hc_schedule_stats(algo, "allreduce", P, n, dt)
+        line = {"name": name, "algo": algo, "dtype": dt, "P": P, "elements_per_rank": n,
+                "steps": st["steps_per_loop"], "two_ceil_log2_P": 2 * math.ceil(math.log2(P)),
+                "launches_step": st["launches_step"], "unit": "us per call"}
+        for mode in ("fused", "step"):
+            opts = B.make_opts(mode)
+
+            def call():
+                B.hc_allreduce(ptrs, ptrs, P, n, dt, "sum", algo, opts, sh)
+            for _ in range(5):
+                call()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            line[mode + "_eager_us"] = round(e0.elapsed_time(e1) / reps * 1e3, 2)
+            hold_device(reps)
+            e0.record(stream)
+            for _ in range(reps):
+                call()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            line[mode + "_queued_us"] = round(e0.elapsed_time(e1) / reps * 1e3, 2)
+            g = B.Graph()
+            for _ in range(reps):
+                g.add_allreduce(ptrs, ptrs, P, n, dt, "sum", algo, opts)
+            g.build()
+            g.launch(sh)
+            torch.cuda.synchronize()
+            e0.record(stream)
+            g.launch(sh)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            line[mode + "_graph_us"] = round(e0.elapsed_time(e1) / reps * 1e3, 2)
+            g.close()
+        out.append(line)
+    return out
+
+
 def run_ours(args, w):
     import torch
     import torch.distributed as dist
@@ -282,34 +531,16 @@ def run_ours(args, w):
 
     P, n, dt = w["P"], w["n"], w["dtype"]
     b = ESIZE[dt]
-    tdt = {"float32": torch.float32, "bfloat16": torch.int16, "int32": torch.int32}[dt]
     X = inputs_for(w)
     Xt = torch.from_numpy(X.view(np.int16) if dt == "bfloat16" else X)
-    send = Xt.to(dev)
-    recv = torch.empty_like(send)
-    send_p = [send[r].data_ptr() for r in range(P)]
-    recv_p = [recv[r].data_ptr() for r in range(P)]
-    if w["coll"] == "reducescatter":
-        segs = [B.hc_segment_range(w["algo"], w["coll"], P, n, dt, k) for k in range(P)]
-        rs_out = [torch.empty(max(ln, 8), dtype=tdt, device=dev) for _, ln in segs]
-        recv_p = [t.data_ptr() for t in rs_out]
-    if w["coll"] == "allgather":
-        segs = [B.hc_segment_range(w["algo"], w["coll"], P, n, dt, k) for k in range(P)]
-        ag_in = [send[k, off:off + ln].clone() for k, (off, ln) in enumerate(segs)]
-        send_p = [t.data_ptr() for t in ag_in]
-    opts = B.make_opts(w["mode"], ranks_per_server=w["p_intra"], max_loop_bytes=w["loop_bytes"])
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    stats, _ = B.hc_schedule_stats(w["algo"], w["coll"], P, n, dt, w["p_intra"], w["loop_bytes"])
-    launches = stats["launches_fused"] if w["mode"] == "fused" else stats["launches_step"]
-
-    def call():
-        if w["coll"] == "allreduce":
-            B.hc_allreduce(send_p, recv_p, P, n, dt, w["op"], w["algo"], opts, sh)
-        elif w["coll"] == "reducescatter":
-            B.hc_reduce_scatter(send_p, recv_p, P, n, dt, w["op"], w["algo"], opts, sh)
-        else:
-            B.hc_allgather(send_p, recv_p, P, n, dt, w["algo"], opts, sh)
+    coll = Collective(B, w, Xt.to(dev), sh)
+    send, recv, rs_out, ag_in, segs, call = coll.send, coll.recv, coll.rs_out, coll.ag_in, coll.segs, coll
+    if w["mode"] == "fused":
+        launches, step_bytes = 1, None
+    else:
+        launches, step_bytes = step_call_stats(B, w)
 
     # warm-up, then a sustained run of the same step while clocks are sampled
     for _ in range(args.warmup):
@@ -438,16 +669,23 @@ def run_ours(args, w):
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(w, budget_s=10.0)
 
+    # every other configuration of the benchmark, with clocks sampled over
+    # the whole sweep (one GPU only: replicas would repeat it)
+    configs = configs_clocks = None
+    if world == 1 and not args.no_configs:
+        del coll, send, recv, rs_out, ag_in, call
+        torch.cuda.empty_cache()
+        sweep_sampler = ClockSampler(uuid)
+        configs = config_sweep(args, dev)
+        configs_clocks = sweep_sampler.stop()
+
     if world > 1:
         dist.barrier()
         dist.destroy_process_group()
     if rank != 0:
         return
     peak, peak_kind = measured_peak()
-    if w["mode"] == "fused":
-        alg = algorithmic_bytes(w)
-    else:
-        alg = stats["step_bytes"]
+    alg = algorithmic_bytes(w) if w["mode"] == "fused" else step_bytes
     achieved = alg / (kern_avg * 1e-3) / 1e9
     traffic = traffic_from_profiles(args.workload)
     line = {
@@ -479,6 +717,8 @@ def run_ours(args, w):
         "e2e": e2e,
         "gpu_launches": args.steps * launches,
         "clocks": clocks,
+        "configs": configs,
+        "configs_clocks": configs_clocks,
     }
     print(json.dumps(line), flush=True)
 
@@ -684,12 +924,16 @@ def sweep_small(args):
 
 def sweep_select(args):
     """For each (collective, P, ranks per server, n, mode) time every
-    candidate schedule eagerly (back-to-back calls, CUDA events) and compare
-    the cost model's choice and prediction with the measured best."""
+    candidate schedule and compare the cost model's choice and prediction
+    with the measured best.  Each candidate's time is the device time per
+    call of calls queued behind a spin kernel (the cost model predicts for a
+    caller whose launches keep the device busy), the best of three rounds
+    that visit the candidates in turn."""
     import torch
     from collective_communication_algorithms_gb300 import _binding as B
     torch.cuda.set_device(0)
     B.lib()
+    dev = torch.device("cuda", 0)
     stream = torch.cuda.current_stream()
     sh = stream.cuda_stream
     cases = []
@@ -699,53 +943,20 @@ def sweep_select(args):
                 for mode in ("step", "fused"):
                     cases.append((coll, P, rps, n, mode))
     for coll, P, rps, n, mode in cases:
-        X = hc_inputs.gradients_f32(P, n, seed=0, scale=1e-3)
-        dev = torch.from_numpy(X).cuda()
-        out = torch.empty_like(dev)
+        X = torch.from_numpy(hc_inputs.gradients_f32(P, n, seed=0, scale=1e-3)).to(dev)
         cands = ["ring", "rhd"] + (["pipeline"] if rps > 1 else []) + \
             (["hier"] if rps > 1 and coll == "allreduce" else [])
         pick, pred = B.hc_select_algo(coll, P, n, "float32", mode, rps)
-        reps = 200 if n <= 262144 else 20
-        meas = {}
+        calls = {}
         for algo in cands:
-            r_ps = rps if algo in ("pipeline", "hier") else 1
-            segs = [B.hc_segment_range(algo, coll, P, n, "float32", k) for k in range(P)] \
-                if coll != "allreduce" else None
-            send = [dev[r].data_ptr() for r in range(P)]
-            if coll == "allreduce":
-                recv = [out[r].data_ptr() for r in range(P)]
-            elif coll == "reducescatter":
-                recv = [out[r].data_ptr() for r in range(P)]
-            else:
-                send = [dev[r].data_ptr() + segs[r][0] * 4 for r in range(P)]
-                recv = [out[r].data_ptr() for r in range(P)]
-            scratch = None
-            sb = 0
-            if coll == "reducescatter" and mode == "step":
-                sb = B.hc_scratch_bytes(algo, P, n, "float32")
-                scratch = torch.empty(sb, dtype=torch.uint8, device="cuda")
-            opts = B.make_opts(mode, ranks_per_server=r_ps,
-                               scratch=scratch.data_ptr() if scratch is not None else 0,
-                               scratch_bytes=sb)
-
-            def call():
-                if coll == "allreduce":
-                    B.hc_allreduce(send, recv, P, n, "float32", "sum", algo, opts, sh)
-                elif coll == "reducescatter":
-                    B.hc_reduce_scatter(send, recv, P, n, "float32", "sum", algo, opts, sh)
-                else:
-                    B.hc_allgather(send, recv, P, n, "float32", algo, opts, sh)
-            for _ in range(5):
-                call()
-            torch.cuda.synchronize()
-            e0 = torch.cuda.Event(enable_timing=True)
-            e1 = torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            for _ in range(reps):
-                call()
-            e1.record(stream)
-            torch.cuda.synchronize()
-            meas[algo] = e0.elapsed_time(e1) / reps * 1e3
+            w = dict(algo=algo, coll=coll, P=P, n=n, dtype="float32", op="sum", mode=mode,
+                     p_intra=rps if algo in ("pipeline", "hier") else 1, loop_bytes=0)
+            calls[algo] = Collective(B, w, X, sh)
+        reps = 100 if n <= 262144 else 20
+        meas = {a: float("inf") for a in cands}
+        for _ in range(3):
+            for algo in cands:
+                meas[algo] = min(meas[algo], time_queued(calls[algo], reps, stream))
         best = min(meas, key=meas.get)
         line = {"sweep": "select", "collective": coll, "P": P, "ranks_per_server": rps,
                 "elements_per_rank": n, "mode": mode, "selected": pick,
@@ -753,6 +964,8 @@ def sweep_select(args):
                 "measured_best": best,
                 "selected_over_best": round(meas[pick] / meas[best], 3)}
         print(json.dumps(line), flush=True)
+        del calls, X
+        torch.cuda.empty_cache()
 
 
 def sweep_hostlink(args):

@@ -59,8 +59,8 @@ hc_status_t read_opts(const hc_opts_t* o, hc_algo_t algo, int P, Opts* out) {
     return HC_OK;
 }
 
-// true when some two intervals overlap (empty intervals ignored)
-bool any_overlap(std::vector<Interval> v) {
+// true when some two intervals overlap (empty intervals ignored); sorts v
+bool any_overlap(std::vector<Interval>& v) {
     v.erase(std::remove_if(v.begin(), v.end(), [](const Interval& x) { return x.hi <= x.lo; }),
             v.end());
     std::sort(v.begin(), v.end(), [](const Interval& a, const Interval& b) { return a.lo < b.lo; });
@@ -206,6 +206,9 @@ hc_status_t prepare(hc_coll_t coll, const void* const* send, void* const* recv, 
 
     std::memset(&c.al, 0, sizeof c.al);
     std::vector<Interval> iv;
+    iv.reserve(2 * (size_t)P + 1);  // one allocation each, not one per growth
+    c.reads.reserve((size_t)P);
+    c.writes.reserve((size_t)P + 1);
     const uintptr_t full = (uintptr_t)n * es;
     for (int r = 0; r < P; r++) {
         const uintptr_t d = (uintptr_t)recv[r];

@@ -134,6 +134,19 @@ __device__ __forceinline__ void st_elem(uintptr_t p, uint32_t v) {
 }
 __device__ __forceinline__ uint4 ld_vec(uintptr_t p) { return *(const uint4*)p; }
 __device__ __forceinline__ void st_vec(uintptr_t p, const uint4& v) { *(uint4*)p = v; }
+// the same with an L2 eviction-priority policy (createpolicy)
+__device__ __forceinline__ uint4 ld_vec_hint(uintptr_t p, uint64_t policy) {
+    uint4 v;
+    asm volatile("ld.global.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p), "l"(policy));
+    return v;
+}
+__device__ __forceinline__ void st_vec_hint(uintptr_t p, const uint4& v, uint64_t policy) {
+    asm volatile("st.global.L2::cache_hint.v4.u32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w), "l"(policy)
+                 : "memory");
+}
 // streaming variants for data touched once by the fused kernels
 __device__ __forceinline__ uint4 ld_stream(uintptr_t p) { return __ldcs((const uint4*)p); }
 __device__ __forceinline__ void st_stream(uintptr_t p, const uint4& v) { __stcs((uint4*)p, v); }
@@ -200,6 +213,14 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, uintptr_t gsrc, unsigne
         "l"(gsrc), "r"(bytes), "r"(smem_addr(m))
         : "memory");
 }
+__device__ __forceinline__ void bulk_g2s_hint(void* smem_dst, uintptr_t gsrc, unsigned bytes, uint64_t* m,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_addr(smem_dst)),
+        "l"(gsrc), "r"(bytes), "r"(smem_addr(m)), "l"(policy)
+        : "memory");
+}
 __device__ __forceinline__ void bulk_s2g(uintptr_t gdst, const void* smem_src, unsigned bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
                  "r"(smem_addr(smem_src)), "r"(bytes)
@@ -212,10 +233,16 @@ __device__ __forceinline__ void bulk_s2g_hint(uintptr_t gdst, const void* smem_s
                  "r"(smem_addr(smem_src)), "r"(bytes), "l"(policy)
                  : "memory");
 }
-// Policy: lines written through it are the first evicted from L2.
+// Policies: lines accessed through them are the first (the last) evicted
+// from L2.
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_evict_last_policy() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }

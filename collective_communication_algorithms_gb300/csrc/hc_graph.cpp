@@ -8,11 +8,12 @@
 // Here a node is a validated collective call (the same checks as the eager
 // entry points).  Dependencies: node j waits for node i < j when one writes a
 // device byte range the other reads or writes; independent nodes become
-// parallel branches.  Build captures each node's kernel launches into a
-// child CUDA graph (stream capture on a private stream) and instantiates the
-// whole DAG; launch replays it on the caller's stream with one call, so the
-// per-launch host overhead of step mode and of chains of small collectives
-// is paid once per build.
+// parallel branches.  Build captures every node's kernel launches in one
+// stream capture over private streams (one per lane of the DAG, joined by
+// events) and instantiates the graph; launch replays it on the caller's
+// stream with one call, so the per-launch host overhead of step mode and of
+// chains of small collectives is paid once per build.
+#include <algorithm>
 #include <new>
 #include <vector>
 
@@ -96,38 +97,91 @@ hc_status_t hc_graph_add_broadcast(hc_graph_t g, const void* send, void* const* 
 hc_status_t hc_graph_build(hc_graph_t g) {
     if (!g) return HC_ERR_INVALID_ARG;
     release(g);
-    cudaStream_t cs = nullptr;
-    cudaError_t e = cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking);
-    if (e != cudaSuccess) return HC_ERR_CUDA;
-    e = cudaGraphCreate(&g->graph, 0);
-    std::vector<cudaGraphNode_t> gn(g->nodes.size());
-    hc_status_t st = e == cudaSuccess ? HC_OK : HC_ERR_CUDA;
-    for (size_t j = 0; j < g->nodes.size() && st == HC_OK; j++) {
-        cudaGraph_t child = nullptr;
-        if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
-            st = HC_ERR_CUDA;
-            break;
+    const int N = (int)g->nodes.size();
+    // Lanes: collective j continues the lane of its latest dependency when
+    // no other collective has continued that one yet (it is then that lane's
+    // last collective, so stream order adds no dependency the DAG lacks);
+    // otherwise it opens a lane of its own.  Each lane is captured on its own
+    // stream, so consecutive dependent collectives keep the programmatic
+    // (PDL) edges between their launches, and independent ones become
+    // parallel branches.
+    std::vector<int> lane(N), tail;
+    std::vector<char> continued(N, 0);
+    for (int j = 0; j < N; j++) {
+        int L = -1;
+        if (!g->deps[j].empty()) {
+            const int i = g->deps[j].back();
+            if (!continued[i]) {
+                continued[i] = 1;
+                L = lane[i];
+            }
         }
-        const hc_status_t xs = execute(g->nodes[j], cs);
-        const cudaError_t ce = cudaStreamEndCapture(cs, &child);
-        if (xs != HC_OK || ce != cudaSuccess || !child) {
-            if (child) cudaGraphDestroy(child);
-            st = xs != HC_OK ? xs : HC_ERR_CUDA;
-            break;
+        if (L < 0) {
+            L = (int)tail.size();
+            tail.push_back(j);
         }
-        size_t nk = 0;
-        cudaGraphGetNodes(child, nullptr, &nk);
-        g->kernels += (int)nk;
-        std::vector<cudaGraphNode_t> d;
-        for (int i : g->deps[j]) d.push_back(gn[i]);
-        e = cudaGraphAddChildGraphNode(&gn[j], g->graph, d.data(), d.size(), child);
-        cudaGraphDestroy(child);
-        if (e != cudaSuccess) st = HC_ERR_CUDA;
+        lane[j] = L;
+        tail[L] = j;
     }
-    if (st == HC_OK && cudaGraphInstantiate(&g->exec, g->graph, 0) != cudaSuccess) st = HC_ERR_CUDA;
-    cudaStreamDestroy(cs);
-    if (st != HC_OK) release(g);
-    return st;
+    const int nl = std::max<int>(1, (int)tail.size());
+    std::vector<cudaStream_t> st(nl, nullptr);
+    std::vector<cudaEvent_t> done(N, nullptr);
+    cudaEvent_t fork = nullptr;
+    hc_status_t rc = HC_OK;
+    auto ok = [&](cudaError_t e) {
+        if (e != cudaSuccess && rc == HC_OK) rc = HC_ERR_CUDA;
+        return rc == HC_OK;
+    };
+    for (int l = 0; l < nl && ok(cudaSuccess); l++) ok(cudaStreamCreateWithFlags(&st[l], cudaStreamNonBlocking));
+    for (int j = 0; j < N && rc == HC_OK; j++) ok(cudaEventCreateWithFlags(&done[j], cudaEventDisableTiming));
+    if (rc == HC_OK) ok(cudaEventCreateWithFlags(&fork, cudaEventDisableTiming));
+    bool capturing = false;
+    if (rc == HC_OK && ok(cudaStreamBeginCapture(st[0], cudaStreamCaptureModeThreadLocal))) {
+        capturing = true;
+        ok(cudaEventRecord(fork, st[0]));
+        for (int l = 1; l < nl && rc == HC_OK; l++) ok(cudaStreamWaitEvent(st[l], fork, 0));
+        for (int j = 0; j < N && rc == HC_OK; j++) {
+            cudaStream_t s = st[lane[j]];
+            for (int i : g->deps[j])
+                if (lane[i] != lane[j] && !ok(cudaStreamWaitEvent(s, done[i], 0))) break;
+            if (rc != HC_OK) break;
+            const hc_status_t xs = execute(g->nodes[j], s);
+            if (xs != HC_OK) {
+                rc = xs;
+                break;
+            }
+            ok(cudaEventRecord(done[j], s));
+        }
+        for (int l = 1; l < nl && rc == HC_OK; l++) ok(cudaStreamWaitEvent(st[0], done[tail[l]], 0));
+    }
+    if (capturing) {
+        cudaGraph_t graph = nullptr;
+        const cudaError_t ce = cudaStreamEndCapture(st[0], &graph);
+        if (rc == HC_OK && (ce != cudaSuccess || !graph)) rc = HC_ERR_CUDA;
+        if (rc == HC_OK) g->graph = graph;
+        else if (graph) cudaGraphDestroy(graph);
+    }
+    if (rc == HC_OK) {
+        size_t nn = 0;
+        cudaGraphGetNodes(g->graph, nullptr, &nn);
+        std::vector<cudaGraphNode_t> all(nn);
+        if (nn) cudaGraphGetNodes(g->graph, all.data(), &nn);
+        for (cudaGraphNode_t v : all) {
+            cudaGraphNodeType t;
+            if (cudaGraphNodeGetType(v, &t) == cudaSuccess && t == cudaGraphNodeTypeKernel) g->kernels++;
+        }
+        if (cudaGraphInstantiate(&g->exec, g->graph, 0) != cudaSuccess) rc = HC_ERR_CUDA;
+    }
+    if (fork) cudaEventDestroy(fork);
+    for (cudaEvent_t e : done)
+        if (e) cudaEventDestroy(e);
+    for (cudaStream_t s : st)
+        if (s) cudaStreamDestroy(s);
+    if (rc != HC_OK) {
+        cudaGetLastError();  // leave no pending error behind for the caller
+        release(g);
+    }
+    return rc;
 }
 
 hc_status_t hc_graph_launch(hc_graph_t g, hc_stream_t stream) {

@@ -69,9 +69,13 @@ struct DevItem {
     int16_t out_base, out_rot, out_mod, out_cnt;
     int16_t in_base, in_rot, in_mod, in_cnt;
     int16_t acc_rank;  // -1 = none
-    uint8_t acc_loc, in_loc, out_loc, pad0;
+    uint8_t acc_loc, in_loc, out_loc;
+    uint8_t early;     // 1: no launch of the call writes the inputs (out-of-place
+                       // ranks' own inputs), so they may be loaded before the
+                       // wait on the previous launch (see StepParams::early)
     int16_t seg_width, seg_reps;
-    int16_t pad1;
+    int16_t once;      // 1: no other item of the launch reads this item's inputs or
+                       // accumulator, so its loads may leave L2 first
     int32_t seg_first, seg_stride;
     int32_t cta_begin;  // first CTA of this item in the launch grid
 };
@@ -89,6 +93,12 @@ struct StepParams {
     unsigned long long wait_ns;  // TMA-staged step kernel: limit of the first mbarrier wait
     int* err;         // TMA-staged step kernel: device error flag (HC_ERR_TIMEOUT)
     int32_t hold;     // TMA-staged step kernel: wait-expiry test mode
+    int32_t early;    // 1: not the call's first launch, so every kernel launched
+                      // before this call has completed once this grid runs at all
+                      // (each earlier launch of the call waited for its
+                      // predecessor before letting its dependents start): items
+                      // flagged `early` may load their inputs before the
+                      // programmatic wait on the previous launch
     int32_t nitems;
     int32_t total_ctas;
     DevItem items[MAXI];

@@ -68,6 +68,14 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
     const int64_t nthreads = (int64_t)(cend - I.cta_begin) * blockDim.x;
     const int64_t t0 = (int64_t)(b - I.cta_begin) * blockDim.x + threadIdx.x;
     const int nseg = I.seg_width * I.seg_reps;
+    // Operands no other item of this launch reads are loaded with an L2
+    // evict-first policy, so that what stays in L2 is what the next steps
+    // read again (this step's outputs).  On GB300 this took the Ring
+    // AllReduce fp32 step mode from 0.94 to 1.15 of the copy bandwidth on its
+    // own bytes (the accumulators then come from L2), the Ring
+    // ReduceScatter / AllGather steps from 0.84 / 0.85 to 0.99.
+    const uint64_t first_out = l2_evict_first_policy();
+    auto ld_vec = [&](uintptr_t a) -> uint4 { return I.once ? ld_vec_hint(a, first_out) : hc::ld_vec(a); };
     // Programmatic dependent launch: this grid may be scheduled while the
     // previous step's grid drains.  Wait for that grid to complete (and its
     // writes to be visible) before touching any buffer, then let the next
@@ -195,29 +203,48 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
     const int64_t send_ = sbeg + p.L < p.n ? sbeg + p.L : p.n;
     const int64_t hi = sbeg + p.hi < send_ ? sbeg + p.hi : send_;
     const int64_t lo = sbeg + p.lo;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (lo >= hi) return;  // the slice misses this (short) segment
-    const int64_t nfull = (hi - lo) / A;
+    const int64_t nfull = lo < hi ? (hi - lo) / A : 0;
     const int64_t t0 = tile * kTmaTile;
     const int acc_slot = I.acc_rank >= 0 ? I.in_cnt : -1;
     const int nops = I.in_cnt + (acc_slot >= 0 ? 1 : 0);
-    if (t0 < nfull * 16) {
-        const int64_t left = nfull * 16 - t0;
-        const unsigned tb = (unsigned)(left < kTmaTile ? left : kTmaTile);
-        const uintptr_t off = (uintptr_t)lo * ES + (uintptr_t)t0;
-        uint64_t* full = (uint64_t*)(smem + (size_t)nops * kTmaTile);
+    const bool staged = t0 < nfull * 16;
+    const int64_t left = nfull * 16 - t0;
+    const unsigned tb = (unsigned)(left < kTmaTile ? left : kTmaTile);
+    const uintptr_t off = (uintptr_t)lo * ES + (uintptr_t)t0;
+    uint64_t* full = (uint64_t*)(smem + (size_t)nops * kTmaTile);
+    // Inputs that no launch of this call writes may be requested before the
+    // programmatic wait, overlapping the previous launch's tail; everything
+    // else (the accumulator, every store) comes after it.
+    const bool early = staged && p.early && I.early;
+    // L2 policies as in step_kernel: operands read by this item only leave
+    // L2 first; the outputs, which the next step reads, leave it last (on
+    // GB300 the Pipeline 4 x 8 step mode went from 0.82 to 0.86 of the copy
+    // bandwidth on its own bytes, the hierarchical from 0.92 to 0.94)
+    const uint64_t first_out = l2_evict_first_policy();
+    auto load = [&](int slot, uintptr_t src) {
+        if (I.once) bulk_g2s_hint(smem + (size_t)slot * kTmaTile, src, tb, full, first_out);
+        else bulk_g2s(smem + (size_t)slot * kTmaTile, src, tb, full);
+    };
+    auto issue_inputs = [&]() {
+        int r = I.in_rot;
+        for (int j = 0; j < I.in_cnt; j++) {
+            load(j, p.base[I.in_loc][I.in_base + r] + off);
+            if (++r == I.in_mod) r = 0;
+        }
+    };
+    if (staged && threadIdx.x == 0) {
+        mbar_init(full, 1 + p.hold);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(full, tb * (unsigned)nops);
+        if (early) issue_inputs();
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (lo >= hi) return;  // the slice misses this (short) segment
+    if (staged) {
         if (threadIdx.x == 0) {
-            mbar_init(full, 1 + p.hold);
-            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-            mbar_arrive_expect_tx(full, tb * (unsigned)nops);
-            int r = I.in_rot;
-            for (int j = 0; j < I.in_cnt; j++) {
-                bulk_g2s(smem + (size_t)j * kTmaTile, p.base[I.in_loc][I.in_base + r] + off, tb, full);
-                if (++r == I.in_mod) r = 0;
-            }
-            if (acc_slot >= 0)
-                bulk_g2s(smem + (size_t)acc_slot * kTmaTile, p.base[I.acc_loc][I.acc_rank] + off, tb, full);
+            if (!early) issue_inputs();
+            if (acc_slot >= 0) load(acc_slot, p.base[I.acc_loc][I.acc_rank] + off);
         }
         __syncthreads();  // the mbarrier is initialised before anyone polls it
         if (!mbar_wait_bounded(full, 0, p.wait_ns)) {
@@ -230,9 +257,10 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
             for (int j = 1; j < I.in_cnt; j++)
                 v = vop<DT, OP>(v, *(const uint4*)(smem + (size_t)j * kTmaTile + vo));
             if (acc_slot >= 0) v = vop<DT, OP>(*(const uint4*)(smem + (size_t)acc_slot * kTmaTile + vo), v);
+            const uint64_t last_out = l2_evict_last_policy();
             int o = I.out_rot;
             for (int j = 0; j < I.out_cnt; j++) {
-                st_vec(p.base[I.out_loc][I.out_base + o] + off + vo, v);
+                st_vec_hint(p.base[I.out_loc][I.out_base + o] + off + vo, v, last_out);
                 if (++o == I.out_mod) o = 0;
             }
         }
@@ -501,11 +529,12 @@ int resident_blocks(void* fn) {
 constexpr int kSmallItems = 48;   // parameter block under 4 KB
 constexpr int kLargeItems = 256;  // large kernel parameter block
 
+// early: not the call's first kernel launch (StepParams::early)
 template <int MAXI>
 cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t first, size_t count,
                               hc_dtype_t dt, hc_op_t op,
                               const uintptr_t (&base)[LOC_COUNT][kMaxRanks],
-                              cudaStream_t stream, int sm_count, bool host_buffers) {
+                              cudaStream_t stream, int sm_count, bool host_buffers, bool early) {
     static thread_local StepParams<MAXI> p;  // large: keep it off the stack
     std::memcpy(p.base, base, sizeof(p.base));
     p.L = plan.lay.L;
@@ -514,6 +543,7 @@ cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t firs
     p.hi = L.hi;
     p.vecs = (L.hi - L.lo + plan.lay.A - 1) / plan.lay.A;
     p.tiles = 0;
+    p.early = early ? 1 : 0;
     p.hold = g_test_expire_waits.load() ? 1 : 0;
     p.wait_ns = p.hold ? kTestWaitLimitNs : kWaitLimitNs;
     p.err = nullptr;
@@ -562,18 +592,20 @@ cudaError_t launch_step(const Plan& plan, int P, hc_dtype_t dt, hc_op_t op,
                         int sm_count, bool host_buffers) {
     (void)P;
     uint64_t index = 0;
+    int kernels = 0;  // kernel launches of this call so far
     for (const PlanLaunch& L : plan.launches) {
         const TraceRange range("hc step launch", 0, index++);
         size_t ni = L.items.size();
         cudaError_t e = cudaSuccess;
         if (ni <= (size_t)kSmallItems) {
             e = launch_step_items<kSmallItems>(plan, L, 0, ni, dt, op, base, stream, sm_count,
-                                               host_buffers);
+                                               host_buffers, kernels++ > 0);
         } else {
             // items of one step are independent, so a step may be split
             for (size_t f = 0; f < ni && e == cudaSuccess; f += kLargeItems)
                 e = launch_step_items<kLargeItems>(plan, L, f, std::min(ni - f, (size_t)kLargeItems),
-                                                   dt, op, base, stream, sm_count, host_buffers);
+                                                   dt, op, base, stream, sm_count, host_buffers,
+                                                   kernels++ > 0);
         }
         if (e != cudaSuccess) return e;
     }
@@ -664,11 +696,10 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     // shared memory per block), one block per kTmaTile bytes of a segment.
     // Against the register path on GB300 (fraction of the measured copy
     // bandwidth, same call): Pipeline fp32 4x8 1.007 vs 0.953, hierarchical
-    // 0.994 vs 0.930, Ring ReduceScatter fp32 1.010 vs 0.964; Ring fp32 and
-    // bf16 and RHD bf16 sum AllReduce within 0.2 %; RHD bf16 max 0.989 vs
-    // 1.005, so bf16 max / min up to 16 ranks keep the register path.
-    const bool bf16_maxmin = es == 2 && (a.op == HC_MAX || a.op == HC_MIN);
-    if (!a.host_buffers && a.P <= kTmaMaxRanks && !(bf16_maxmin && a.P <= 16)) {
+    // 0.994 vs 0.930, Ring ReduceScatter fp32 1.010 vs 0.964, Ring bf16 max
+    // 0.967 vs 0.935, RHD bf16 max 0.990 vs 0.975; Ring fp32 and bf16 and
+    // RHD bf16 sum AllReduce within 0.2 %.
+    if (!a.host_buffers && a.P <= kTmaMaxRanks) {
         void* fn = pick_reduce_tma(a.algo, COLL, a.dtype, a.op, a.P);
         if (fn) {
             p.err = device_error_flag();

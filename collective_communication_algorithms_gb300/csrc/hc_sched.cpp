@@ -30,6 +30,7 @@
 #include <algorithm>
 #include <cstring>
 #include <map>
+#include <tuple>
 
 #include "hc_internal.h"
 
@@ -631,6 +632,43 @@ bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root, in
                 final_items.push_back(make_item(one(q), LOC_WORK, -1, 0, one(q), LOC_ORIG, sp));
         }
     }
+
+    // inputs no launch of this call writes: the original buffers of ranks
+    // that are out of place (every output goes to LOC_WORK or LOC_FINAL)
+    auto mark_early = [&](std::vector<DevItem>& items) {
+        for (DevItem& it : items) {
+            bool ok = it.in_loc == LOC_ORIG;
+            for (int j = 0; ok && j < it.in_cnt; j++)
+                ok = !alias.orig_is_work[it.in_base + (it.in_rot + j) % it.in_mod];
+            it.early = ok ? 1 : 0;
+        }
+    };
+    for (auto& items : bound) mark_early(items);
+    mark_early(final_items);
+
+    // operands read by one item of a launch only: the kernels load them with
+    // an L2 evict-first policy (what stays in L2 is then what later steps
+    // read again); an operand two items read (the Pipeline AllGather forwards
+    // a block and broadcasts it in the same step) keeps the normal policy
+    auto mark_once = [&](std::vector<DevItem>& items) {
+        std::map<std::tuple<int, int, int>, int> reads;  // (location, rank, segment) -> items
+        auto each = [&](const DevItem& it, auto&& fn) {
+            for (int i = 0; i < it.seg_width * it.seg_reps; i++) {
+                const int k = it.seg_first + (i / it.seg_width) * it.seg_stride + i % it.seg_width;
+                for (int j = 0; j < it.in_cnt; j++)
+                    fn(std::make_tuple((int)it.in_loc, it.in_base + (it.in_rot + j) % it.in_mod, k));
+                if (it.acc_rank >= 0) fn(std::make_tuple((int)it.acc_loc, (int)it.acc_rank, k));
+            }
+        };
+        for (const DevItem& it : items) each(it, [&](const std::tuple<int, int, int>& t) { reads[t]++; });
+        for (DevItem& it : items) {
+            bool once = true;
+            each(it, [&](const std::tuple<int, int, int>& t) { once = once && reads[t] == 1; });
+            it.once = once ? 1 : 0;
+        }
+    };
+    for (auto& items : bound) mark_once(items);
+    mark_once(final_items);
 
     if (plan.lay.n == 0) return true;
     for (int lp = 0; lp < plan.sl.loops; lp++) {
