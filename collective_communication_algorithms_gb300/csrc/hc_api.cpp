@@ -542,13 +542,21 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
 hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t count,
                            hc_dtype_t dtype, hc_mode_t mode, hc_algo_t* out_algo,
                            double* predicted_us) {
-    // measured on GB300 (bench.py workloads and the small-message sweep):
-    // host cost of a call and of each of its launches, device time per
-    // dependent launch, HBM bandwidth and the fraction of it step / fused
-    // kernels reach (measured on GB300; step kernels launched with programmatic
-    // stream serialization, fused kernels TMA-staged, one block per tile)
-    const double kHostCallUs = 3.5, kHostLaunchUs = 2.3, kDeviceStepUs = 3.0;
-    const double kBandwidth = 6800e9, kStepFrac = 0.9, kFusedFrac = 1.0;
+    // Constants measured on GB300 (a C caller; bench.py --sweep select, the
+    // benchmark's configurations and a C timing loop around the entry points):
+    //  host: 0.55 us of the library's own work per call, 1.4 us per launch;
+    //  step mode: 2.8 us of device time per dependent launch, and the
+    //    fraction of the copy bandwidth each schedule's steps reach on their
+    //    own bytes (Ring above 1: its partial sums come back from L2);
+    //  fused mode: a fixed device cost per call that grows with the ranks a
+    //    block reduces (1.55 us + per-rank cost of the schedule's reduction:
+    //    the Ring chain, the RHD tree -- compile-time below 16 ranks, looped
+    //    above --, the Pipeline and hierarchical two-level trees, the
+    //    AllGather's plain copies), then the bytes at the path's fraction of
+    //    the bandwidth (AllReduce / ReduceScatter TMA-staged up to 32 ranks;
+    //    AllGather register path below 16 ranks, TMA-staged above).
+    const double kHostCallUs = 0.55, kHostLaunchUs = 1.4, kStepLaunchUs = 2.8;
+    const double kFusedBaseUs = 1.55, kBandwidth = 6800e9;
     if (!out_algo || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
     if (mode != HC_MODE_FUSED && mode != HC_MODE_STEP) return HC_ERR_INVALID_ARG;
     if (P < 1 || P > kMaxRanks) return HC_ERR_INVALID_ARG;
@@ -557,7 +565,8 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
     const bool servers = ranks_per_server > 1 && P % ranks_per_server == 0;
     if (servers && coll != HC_COLL_BROADCAST) cands.push_back(HC_ALGO_PIPELINE);
     if (servers && coll == HC_COLL_ALLREDUCE) cands.push_back(HC_ALGO_HIER);
-    double best = 0;
+    const bool copy = coll == HC_COLL_ALLGATHER || coll == HC_COLL_BROADCAST;
+    double best = 0, best_dev = 0;
     bool have = false;
     for (hc_algo_t a : cands) {
         hc_stats_t st;
@@ -565,16 +574,35 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
         st.struct_size = sizeof st;
         const int rps = (a == HC_ALGO_PIPELINE || a == HC_ALGO_HIER) ? ranks_per_server : 1;
         if (hc_schedule_stats(a, coll, P, rps, count, dtype, 0, &st, nullptr) != HC_OK) continue;
+        double host, dev;
+        if (mode == HC_MODE_STEP) {
+            const double f = a == HC_ALGO_RING ? 1.1 : a == HC_ALGO_RHD ? 1.0 : 0.96;
+            host = kHostCallUs + st.launches_step * kHostLaunchUs;
+            dev = st.launches_step * kStepLaunchUs + (double)st.step_bytes / (f * kBandwidth) * 1e6;
+        } else {
+            double per_rank, f;
+            if (copy) {
+                per_rank = 0.03;
+                f = P < 16 ? 0.94 : 1.02;
+            } else {
+                per_rank = a == HC_ALGO_RING       ? 0.055
+                           : a == HC_ALGO_RHD      ? (P < 16 ? 0.04 : 0.067)
+                           : a == HC_ALGO_PIPELINE ? 0.07
+                                                   : 0.083;
+                f = P <= 32 ? 1.0 : 0.96;
+            }
+            host = kHostCallUs + st.launches_fused * kHostLaunchUs;
+            dev = st.launches_fused ? kFusedBaseUs + per_rank * P +
+                                          (double)st.fused_bytes / (f * kBandwidth) * 1e6
+                                    : 0.0;
+        }
         // launches are queued asynchronously: the host cost and the device
-        // time overlap, the larger one decides
-        const int launches = mode == HC_MODE_STEP ? st.launches_step : st.launches_fused;
-        const double bytes = mode == HC_MODE_STEP ? (double)st.step_bytes : (double)st.fused_bytes;
-        const double frac = mode == HC_MODE_STEP ? kStepFrac : kFusedFrac;
-        const double host = kHostCallUs + launches * kHostLaunchUs;
-        const double device = launches * kDeviceStepUs + bytes / (frac * kBandwidth) * 1e6;
-        const double t = host > device ? host : device;
-        if (!have || t < best) {
+        // time overlap and the larger decides; between equal costs the lower
+        // device time, then the earlier candidate
+        const double t = host > dev ? host : dev;
+        if (!have || t < best || (t == best && dev < best_dev)) {
             best = t;
+            best_dev = dev;
             *out_algo = a;
             have = true;
         }

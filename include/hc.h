@@ -391,15 +391,22 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
  * bytes its kernels move over the HBM bandwidth (beta; the reduction, gamma,
  * hides under the memory traffic).  Launches are queued asynchronously, so
  * the host's launch cost and the device time overlap:
- *   t = max(c_host + launches * alpha_host,
- *           launches * alpha_dev + bytes / (f * B))
- * with launches and bytes (step or fused mode) from hc_schedule_stats and
- * c_host = 3.5 us per call, alpha_host = 2.3 us per launch, alpha_dev =
- * 3.0 us per dependent launch, f = 0.9 (step) / 1.0 (fused), B = 6800 GB/s,
- * all measured on GB300.  Candidates: Ring and RHD;
- * Pipeline and, for an AllReduce, the hierarchical AllReduce when
- * ranks_per_server > 1 divides P.  On a tie the earlier candidate wins (Ring,
- * RHD, Pipeline, hierarchical).
+ *   t = max(c_host + launches * alpha_host, t_device)
+ *   step:  t_device = launches * alpha_step + step_bytes / (f_algo * B)
+ *   fused: t_device = alpha_fused + r_algo * P + fused_bytes / (f_path * B)
+ * with launches and bytes from hc_schedule_stats and, measured on GB300 for
+ * a C caller: c_host = 0.55 us, alpha_host = 1.4 us per launch,
+ * alpha_step = 2.8 us per dependent launch, f_algo = 1.1 (Ring: its partial
+ * sums come back from L2), 1.0 (RHD), 0.96 (Pipeline, hierarchical);
+ * alpha_fused = 1.55 us, r_algo the per-rank cost of the schedule's
+ * reduction in one block (Ring 0.055 us, RHD 0.04 below 16 ranks and 0.067
+ * from 16, Pipeline 0.07, hierarchical 0.083, AllGather / Broadcast 0.03),
+ * f_path = 1.0 (AllReduce / ReduceScatter up to 32 ranks, 0.96 above), 0.94
+ * (AllGather / Broadcast below 16 ranks) or 1.02 (from 16); B = 6800 GB/s.
+ * Candidates: Ring and RHD; Pipeline and, for an AllReduce, the
+ * hierarchical AllReduce when ranks_per_server > 1 divides P; Broadcast:
+ * RHD only.  Between equal costs the lower device time wins, then the
+ * earlier candidate (Ring, RHD, Pipeline, hierarchical).
  *  out_algo      : the cheapest schedule
  *  predicted_us  : its predicted time in microseconds (may be NULL)
  */

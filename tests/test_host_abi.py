@@ -553,17 +553,42 @@ def test_hier_is_allreduce_only():
             B.hc_step_plan("hier", coll, 8, 100, "float32", 4)
 
 
-def test_cost_model_selector():
-    """hc_select_algo: the cheapest schedule under t = max(c_host + launches *
-    alpha_host, launches * alpha_dev + bytes / (f B)), recomputed here from
-    hc_schedule_stats; small messages pick the schedule with the fewest
-    launches; the hierarchical schedule is offered only with servers."""
-    def model(algo, coll, P, n, mode, rps):
-        st, _ = B.hc_schedule_stats(algo, coll, P, n, "float32", rps, 0)
-        L = st["launches_step"] if mode == "step" else st["launches_fused"]
-        by = st["step_bytes"] if mode == "step" else st["fused_bytes"]
-        f = 0.9 if mode == "step" else 1.0
-        return max(3.5 + L * 2.3, L * 3.0 + by / (f * 6800e9) * 1e6)
+def test_cost_model_selector_against_measured_times():
+    """hc_select_algo picks, for each of the 36 cases timed on a GB300
+    (tests/data/selector_sweep_gb300.json, written from `bench.py --sweep
+    select`: AllReduce / ReduceScatter / AllGather x P = 8 and 4 x 8 x
+    4 Ki / 256 Ki / 4 Mi elements per rank x step / fused), a schedule whose
+    measured time is within 3 % of the fastest candidate's in every case and
+    equal to it, within the measurement's own noise, in at least 34 cases.
+    The noise is the largest spread the table shows between candidates that
+    run the identical kernel (the fused AllGather's schedules all run the
+    same kernel on the same segment layout)."""
+    import json
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "data",
+                        "selector_sweep_gb300.json")
+    cases = json.load(open(path))["cases"]
+    assert len(cases) == 36
+    noise = max(max(c["measured_us"].values()) / min(c["measured_us"].values())
+                for c in cases if c["collective"] == "allgather" and c["mode"] == "fused")
+    assert 1.0 <= noise < 1.03
+    within = best = 0
+    for c in cases:
+        m = c["measured_us"]
+        pick, pred = B.hc_select_algo(c["collective"], c["P"], c["elements_per_rank"], "float32",
+                                      c["mode"], c["ranks_per_server"])
+        assert pick in m and pred > 0
+        ratio = m[pick] / min(m.values())
+        within += ratio <= 1.03
+        best += ratio <= noise
+    assert within == 36
+    assert best >= 34, best
+
+
+def test_cost_model_selector_candidates_and_latency_regime():
+    """The hierarchical schedule is offered only with servers, and only for
+    the AllReduce; Broadcast has RHD only; in the latency regime the step
+    mode picks the schedule with the fewest launches (RHD's 2 ceil(log2 P)
+    against Ring's 2 (P - 1))."""
     for coll in ("allreduce", "reducescatter", "allgather"):
         for P, rps in ((2, 1), (5, 1), (8, 1), (12, 4), (16, 4), (32, 8), (64, 8)):
             for n in (256, 4096, 1 << 20, 16 << 20):
@@ -571,15 +596,11 @@ def test_cost_model_selector():
                     algo, t = B.hc_select_algo(coll, P, n, "float32", mode, rps)
                     cands = ["ring", "rhd"] + (["pipeline"] if rps > 1 else []) + \
                         (["hier"] if rps > 1 and coll == "allreduce" else [])
-                    costs = {a: model(a, coll, P, n, mode, rps if a in ("pipeline", "hier") else 1)
-                             for a in cands}
-                    assert algo in cands
-                    assert abs(t - costs[algo]) < 1e-6 * max(1, t)
-                    assert t <= min(costs.values()) + 1e-9
-    # latency regime, step mode: RHD's 2 ceil(log2 P) launches beat Ring's 2 (P - 1)
+                    assert algo in cands and t > 0
     assert B.hc_select_algo("allreduce", 8, 1024, "float32", "step")[0] == "rhd"
     assert B.hc_select_algo("allreduce", 16, 256, "float32", "step")[0] == "rhd"
     assert B.hc_select_algo("broadcast", 8, 1024, "float32", "step")[0] == "rhd"
+    assert B.hc_select_algo("broadcast", 8, 1024, "float32", "fused")[0] == "rhd"
 
 
 def test_plan_cache_under_concurrent_host_threads():
