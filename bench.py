@@ -216,15 +216,16 @@ def hold_device(steps):
 
 
 def traffic_from_profiles(workload):
-    """dram read+write bytes per launch of the dominant kernel from a
-    committed ncu summary, if it was taken on the current kernel source."""
+    """DRAM read + write bytes of one call (fused mode: its one launch; step
+    mode: all its launches) from a committed ncu summary, if it was taken on
+    the current kernel source."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             t = json.load(f)
         e = t.get(workload)
         if e and e.get("kernel_source_sha256_16") == kernel_source_hash():
-            return float(e["dram_bytes_per_launch"])
+            return float(e.get("dram_bytes_per_call", e["dram_bytes_per_launch"]))
     except Exception:
         pass
     return None

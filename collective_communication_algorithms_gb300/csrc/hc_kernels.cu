@@ -252,7 +252,20 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
             return;
         }
         const unsigned vo = threadIdx.x * 16u;
-        if (vo < tb) {
+        if (I.in_cnt == 1 && acc_slot < 0) {
+            // a copy: the tile goes from shared memory to every output by
+            // bulk stores; the block leaves once they have read it
+            if (threadIdx.x == 0) {
+                const uint64_t last_out = l2_evict_last_policy();
+                int o = I.out_rot;
+                for (int j = 0; j < I.out_cnt; j++) {
+                    bulk_s2g_hint(p.base[I.out_loc][I.out_base + o] + off, smem, tb, last_out);
+                    if (++o == I.out_mod) o = 0;
+                }
+                bulk_commit();
+                bulk_wait_read_all();
+            }
+        } else if (vo < tb) {
             uint4 v = *(const uint4*)(smem + vo);
             for (int j = 1; j < I.in_cnt; j++)
                 v = vop<DT, OP>(v, *(const uint4*)(smem + (size_t)j * kTmaTile + vo));
@@ -557,7 +570,18 @@ cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t firs
         operands = std::max(operands, it.in_cnt + (it.acc_rank >= 0 ? 1 : 0));
     }
     p.nitems = (int)count;
-    if (widest >= 3 && operands <= kStepTmaMaxOperands && !host_buffers) {
+    // Launches of pure broadcasts (every item copies one input to three or
+    // more outputs: the mesh AllGather of the hierarchical AllReduce) also
+    // take the TMA-staged kernel, whose bulk stores write a tile from shared
+    // memory to every output: on GB300 the hierarchical 4 x 8 step mode went
+    // from 0.96 to 1.02 of the copy bandwidth on its own bytes.  Launches
+    // that mix such broadcasts with 1 -> 1 forwards of the same blocks (the
+    // Pipeline AllGather steps) measured 0.89 -> 0.77 that way and keep the
+    // register kernel.
+    bool broadcasts = true;
+    for (const DevItem& it : part.items)
+        broadcasts = broadcasts && it.in_cnt == 1 && it.acc_rank < 0 && it.out_cnt >= 3;
+    if ((widest >= 3 || broadcasts) && operands <= kStepTmaMaxOperands && !host_buffers) {
         // TMA-staged: one block per tile of every segment of every item
         void* fn = pick_step_tma<MAXI>(dt, op);
         p.err = device_error_flag();
