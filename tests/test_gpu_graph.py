@@ -114,3 +114,44 @@ def test_graph_replays():
     want = (X.astype(np.int64).sum(0) * P).astype(np.int32)
     assert all(np.array_equal(got[r], want) for r in range(P))
     g.close()
+
+
+@pytest.mark.parametrize("use_graph", [False, True])
+def test_chained_step_calls_read_the_previous_calls_output(use_graph):
+    """Step-mode calls load the inputs no launch of the call writes before
+    waiting for the previous launch (from a call's second launch on).  Two
+    Pipeline 2 x 4 AllReduces (TMA-staged mesh reduce steps) and a
+    hierarchical one, each reading the previous call's output, queued on one
+    stream with no synchronisation in between (eagerly, or as one graph):
+    every result equals the oracle's replay of the chain, bit for bit."""
+    P, n = 8, 70000 + 3
+    npad = (n + 3) // 4 * 4  # rows start on 16-byte boundaries; the calls use n
+    X = hc_inputs.gradients_f32(P, n, seed=41)
+    dev = torch.zeros((P, npad), dtype=torch.float32, device="cuda")
+    dev[:, :n] = torch.from_numpy(X).cuda()
+    A, Bv, C = torch.zeros_like(dev), torch.zeros_like(dev), torch.zeros_like(dev)
+    pipe = B.make_opts("step", ranks_per_server=4, max_loop_bytes=256 << 10)
+    hier = B.make_opts("step", ranks_per_server=4)
+    calls = [(rows(dev), rows(A), "pipeline", pipe), (rows(A), rows(Bv), "pipeline", pipe),
+             (rows(Bv), rows(C), "hier", hier)]
+    stream = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    if use_graph:
+        g = B.Graph()
+        for s, r, algo, opts in calls:
+            g.add_allreduce(s, r, P, n, "float32", "sum", algo, opts)
+        g.build()
+        assert g.info()["edges"] >= 2
+        g.launch(stream)
+        torch.cuda.synchronize()
+        g.close()
+    else:
+        for s, r, algo, opts in calls:
+            B.hc_allreduce(s, r, P, n, "float32", "sum", algo, opts, stream)
+        torch.cuda.synchronize()
+    Y1 = O.replay("pipeline", "allreduce", X, "sum", "float32", p_intra=4, loop_bytes=256 << 10)
+    Y2 = O.replay("pipeline", "allreduce", Y1, "sum", "float32", p_intra=4, loop_bytes=256 << 10)
+    Y3 = O.replay("hier", "allreduce", Y2, "sum", "float32", p_intra=4)
+    for got, want in ((A, Y1), (Bv, Y2), (C, Y3)):
+        assert np.array_equal(got[:, :n].cpu().numpy().view(np.uint32), want.view(np.uint32))
+    assert B.hc_device_status() == 0
