@@ -477,7 +477,7 @@ hc_status_t hc_schedule_stats(hc_algo_t algo, hc_coll_t coll, int P, int ranks_p
                 int64_t lo = std::min(plan.lay.seg_lo(k) + L.lo, plan.lay.seg_hi(k));
                 int64_t hi = std::min(plan.lay.seg_lo(k) + L.hi, plan.lay.seg_hi(k));
                 unsigned long long len = (unsigned long long)(hi - lo) * es;
-                sb += len * (unsigned long long)(it.in_cnt + (it.acc_rank >= 0) + it.out_cnt);
+                sb += len * (unsigned long long)(it.in_cnt + (it.acc_rank >= 0) + item_outputs(it));
             }
     stats->step_bytes = sb;
     const unsigned long long nb = (unsigned long long)n * es;
@@ -525,11 +525,13 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
                     R.in_loc = it.in_loc;
                     R.in_cnt = it.in_cnt;
                     R.out_loc = it.out_loc;
-                    R.out_cnt = it.out_cnt;
+                    R.out_cnt = item_outputs(it);
                     for (int j = 0; j < it.in_cnt; j++)
                         R.in_ranks[j] = it.in_base + (it.in_rot + j) % it.in_mod;
                     for (int j = 0; j < it.out_cnt; j++)
                         R.out_ranks[j] = it.out_base + (it.out_rot + j) % it.out_mod;
+                    for (int j = 0; j < it.out2_cnt; j++)
+                        R.out_ranks[it.out_cnt + j] = it.out2_base + (it.out2_rot + j) % it.out2_mod;
                 }
                 m++;
             }

@@ -59,9 +59,13 @@ Slicing make_slicing(hc_algo_t algo, int P, int p_intra, const Layout& lay, hc_d
 // and every element j of the launch's slice of that segment,
 //     v = in[0][j] (+) in[1][j] (+) ... (+) in[cnt-1][j]      (left to right)
 //     if acc >= 0:  v = acc[j] (+) v                           (received on the left)
-//     out[o][j] = v  for every output o
+//     out[o][j] = v  for every output o of both output sets
 // A copy is an item with one input and no acc.  Rank sets are rotations:
-// member i of (base, rot, mod, cnt) is rank base + (rot + i) % mod.
+// member i of (base, rot, mod, cnt) is rank base + (rot + i) % mod.  The
+// second output set (out2_*, empty when out2_cnt is 0) holds the outputs of
+// another copy of the same input block in the same step, merged into this
+// item so that the block is read once (the Pipeline AllGather forwards a
+// block to the next server and sends it to its own server's ranks).
 // Segment set: seg_first + (i / seg_width) * seg_stride + (i % seg_width),
 // i < seg_width * seg_reps.
 // ---------------------------------------------------------------------------
@@ -78,8 +82,12 @@ struct DevItem {
                        // accumulator, so its loads may leave L2 first
     int32_t seg_first, seg_stride;
     int32_t cta_begin;  // first CTA of this item in the launch grid
+    int16_t out2_base, out2_rot, out2_mod, out2_cnt;
 };
-static_assert(sizeof(DevItem) == 40, "DevItem layout");
+static_assert(sizeof(DevItem) == 48, "DevItem layout");
+
+// Outputs of an item in both output sets.
+inline int item_outputs(const DevItem& it) { return it.out_cnt + it.out2_cnt; }
 
 // Kernel-parameter block of one step launch.  MAXI items at most.
 template <int MAXI>

@@ -52,6 +52,22 @@ constexpr int kStepBatch = 8;  // input loads in flight per vector
 // 0.83 with one, and the hierarchical steps 0.91 against 0.87.
 constexpr int kStepUnroll = 2;
 
+// Calls f(rank) for every output of an item: its output set, then its
+// second output set (a merged copy of the same block).
+template <class F>
+__device__ __forceinline__ void each_output(const DevItem& I, F f) {
+    int o = I.out_rot;
+    for (int j = 0; j < I.out_cnt; j++) {
+        f(I.out_base + o);
+        if (++o == I.out_mod) o = 0;
+    }
+    o = I.out2_rot;
+    for (int j = 0; j < I.out2_cnt; j++) {
+        f(I.out2_base + o);
+        if (++o == I.out2_mod) o = 0;
+    }
+}
+
 // BATCH: input loads issued before reducing (1 for launches whose items
 // have at most two inputs, where 8 blocks per SM give the loads in flight;
 // kStepBatch for wider items, e.g. the Pipeline's intra-server mesh reduce)
@@ -110,13 +126,11 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
 #pragma unroll
                     for (int u = 0; u < kStepUnroll; u++) x[u] = vop<DT, OP>(a[u], x[u]);
                 }
-                int oo = I.out_rot;
-                for (int j = 0; j < I.out_cnt; j++) {
-                    const uintptr_t ob = p.base[I.out_loc][I.out_base + oo];
+                each_output(I, [&](int r) {
+                    const uintptr_t ob = p.base[I.out_loc][r];
 #pragma unroll
                     for (int u = 0; u < kStepUnroll; u++) st_vec(ob + o[u], x[u]);
-                    if (++oo == I.out_mod) oo = 0;
-                }
+                });
                 e += (kStepUnroll - 1) * nthreads * A;  // the loop step adds the last stride
                 continue;
             }
@@ -143,11 +157,7 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
                         if (q < m) v = (c == 0 && q == 0) ? x[0] : vop<DT, OP>(v, x[q]);
                 }
                 if (I.acc_rank >= 0) v = vop<DT, OP>(acc, v);
-                int o = I.out_rot;
-                for (int j = 0; j < I.out_cnt; j++) {
-                    st_vec(p.base[I.out_loc][I.out_base + o] + off, v);
-                    if (++o == I.out_mod) o = 0;
-                }
+                each_output(I, [&](int r) { st_vec(p.base[I.out_loc][r] + off, v); });
             } else {
                 // ragged end of the rank vector: element by element
                 for (int64_t x = e; x < hi; x++) {
@@ -160,11 +170,7 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
                     }
                     if (I.acc_rank >= 0)
                         v = vop<DT, OP>(ld_elem<ES>(p.base[I.acc_loc][I.acc_rank] + xo), v);
-                    int o = I.out_rot;
-                    for (int j = 0; j < I.out_cnt; j++) {
-                        st_elem<ES>(p.base[I.out_loc][I.out_base + o] + xo, v);
-                        if (++o == I.out_mod) o = 0;
-                    }
+                    each_output(I, [&](int r) { st_elem<ES>(p.base[I.out_loc][r] + xo, v); });
                 }
             }
         }
@@ -257,11 +263,7 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
             // bulk stores; the block leaves once they have read it
             if (threadIdx.x == 0) {
                 const uint64_t last_out = l2_evict_last_policy();
-                int o = I.out_rot;
-                for (int j = 0; j < I.out_cnt; j++) {
-                    bulk_s2g_hint(p.base[I.out_loc][I.out_base + o] + off, smem, tb, last_out);
-                    if (++o == I.out_mod) o = 0;
-                }
+                each_output(I, [&](int r) { bulk_s2g_hint(p.base[I.out_loc][r] + off, smem, tb, last_out); });
                 bulk_commit();
                 bulk_wait_read_all();
             }
@@ -271,11 +273,7 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
                 v = vop<DT, OP>(v, *(const uint4*)(smem + (size_t)j * kTmaTile + vo));
             if (acc_slot >= 0) v = vop<DT, OP>(*(const uint4*)(smem + (size_t)acc_slot * kTmaTile + vo), v);
             const uint64_t last_out = l2_evict_last_policy();
-            int o = I.out_rot;
-            for (int j = 0; j < I.out_cnt; j++) {
-                st_vec_hint(p.base[I.out_loc][I.out_base + o] + off + vo, v, last_out);
-                if (++o == I.out_mod) o = 0;
-            }
+            each_output(I, [&](int r) { st_vec_hint(p.base[I.out_loc][r] + off + vo, v, last_out); });
         }
     }
     if (tile == 0 && threadIdx.x == 0) {
@@ -289,11 +287,7 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
                 v = vop<DT, OP>(v, ld_elem<ES>(p.base[I.in_loc][I.in_base + rr] + xo));
             }
             if (acc_slot >= 0) v = vop<DT, OP>(ld_elem<ES>(p.base[I.acc_loc][I.acc_rank] + xo), v);
-            int o = I.out_rot;
-            for (int j = 0; j < I.out_cnt; j++) {
-                st_elem<ES>(p.base[I.out_loc][I.out_base + o] + xo, v);
-                if (++o == I.out_mod) o = 0;
-            }
+            each_output(I, [&](int r) { st_elem<ES>(p.base[I.out_loc][r] + xo, v); });
         }
     }
 }
@@ -571,16 +565,20 @@ cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t firs
     }
     p.nitems = (int)count;
     // Launches of pure broadcasts (every item copies one input to three or
-    // more outputs: the mesh AllGather of the hierarchical AllReduce) also
-    // take the TMA-staged kernel, whose bulk stores write a tile from shared
-    // memory to every output: on GB300 the hierarchical 4 x 8 step mode went
-    // from 0.96 to 1.02 of the copy bandwidth on its own bytes.  Launches
-    // that mix such broadcasts with 1 -> 1 forwards of the same blocks (the
-    // Pipeline AllGather steps) measured 0.89 -> 0.77 that way and keep the
-    // register kernel.
+    // more outputs: the mesh AllGather of the hierarchical AllReduce, the
+    // Pipeline AllGather steps whose forward and intra-server sends of a
+    // block are one item) also take the TMA-staged kernel, whose bulk stores
+    // write a tile from shared memory to every output.  These launches keep
+    // most of their traffic in L2 and were bound by per-thread stores: on
+    // GB300 the hierarchical 4 x 8 step mode went from 0.96 to 1.03 of the
+    // copy bandwidth on its own bytes, the Pipeline 4 x 8 AllReduce step mode
+    // from 0.410 to 0.397 ms per call and its AllGather from 0.223 to 0.208.
+    // Launches that mix broadcasts with 1 -> 1 copies keep the register
+    // kernel (the Pipeline AllGather steps before their sends were merged
+    // measured 0.89 -> 0.77 on bulk copies).
     bool broadcasts = true;
     for (const DevItem& it : part.items)
-        broadcasts = broadcasts && it.in_cnt == 1 && it.acc_rank < 0 && it.out_cnt >= 3;
+        broadcasts = broadcasts && it.in_cnt == 1 && it.acc_rank < 0 && item_outputs(it) >= 3;
     if ((widest >= 3 || broadcasts) && operands <= kStepTmaMaxOperands && !host_buffers) {
         // TMA-staged: one block per tile of every segment of every item
         void* fn = pick_step_tma<MAXI>(dt, op);

@@ -501,7 +501,37 @@ DevItem make_item(const RankSet& outs, uint8_t out_loc, int acc, uint8_t acc_loc
     d.seg_reps = (int16_t)sp.reps;
     d.seg_first = sp.first;
     d.seg_stride = sp.stride;
+    d.out2_mod = 1;  // empty second output set
     return d;
+}
+
+// Merge copies of one step that read the same input block (same location,
+// rank and segments) and write the same location: the second's outputs
+// become the first's second output set, so the block is read once.
+void merge_copies(std::vector<DevItem>& items) {
+    std::vector<DevItem> out;
+    std::vector<char> taken(items.size(), 0);
+    for (size_t i = 0; i < items.size(); i++) {
+        if (taken[i]) continue;
+        DevItem a = items[i];
+        const bool copy = a.in_cnt == 1 && a.acc_rank < 0;
+        for (size_t j = i + 1; copy && a.out2_cnt == 0 && j < items.size(); j++) {
+            const DevItem& b = items[j];
+            if (taken[j] || b.in_cnt != 1 || b.acc_rank >= 0 || b.out2_cnt != 0) continue;
+            if (b.in_loc != a.in_loc || b.out_loc != a.out_loc) continue;
+            if (b.in_base + b.in_rot % b.in_mod != a.in_base + a.in_rot % a.in_mod) continue;
+            if (b.seg_first != a.seg_first || b.seg_width != a.seg_width ||
+                b.seg_reps != a.seg_reps || (a.seg_reps > 1 && b.seg_stride != a.seg_stride))
+                continue;
+            a.out2_base = b.out_base;
+            a.out2_rot = b.out_rot;
+            a.out2_mod = b.out_mod;
+            a.out2_cnt = b.out_cnt;
+            taken[j] = 1;
+        }
+        out.push_back(a);
+    }
+    items.swap(out);
 }
 
 }  // namespace
@@ -611,6 +641,7 @@ bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root, in
         if (si == 0 && coll == HC_COLL_ALLGATHER)
             for (int q = 0; q < P; q++) st_at(q, q) = LOC_WORK;
         if (si == 0 && coll == HC_COLL_BROADCAST) st_at(root, 0) = LOC_WORK;
+        merge_copies(items);
         bound.push_back(items);
     }
 
@@ -743,7 +774,7 @@ int assign_ctas(PlanLaunch& L, const Layout& lay, int threads, int max_ctas) {
         const DevItem& it = L.items[i];
         const int64_t v = item_vectors(it, L, lay);
         need[i] = std::max<int64_t>(1, cdiv(v, threads));
-        weight[i] = std::max<int64_t>(1, v) * (it.in_cnt + (it.acc_rank >= 0 ? 1 : 0) + it.out_cnt);
+        weight[i] = std::max<int64_t>(1, v) * (it.in_cnt + (it.acc_rank >= 0 ? 1 : 0) + item_outputs(it));
         total += need[i];
         wsum += weight[i];
     }
