@@ -55,9 +55,6 @@ constexpr hc_algo_t kAlgoRhdLarge = (hc_algo_t)100;
 __device__ __forceinline__ uint32_t key32(uint32_t u) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
-__device__ __forceinline__ uint32_t key16(uint32_t h) {  // h in the low 16 bits
-    return (h & 0x8000u) ? (~h & 0xFFFFu) : (h | 0x8000u);
-}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t d;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
@@ -89,6 +86,19 @@ struct WordOp<HC_FLOAT32, OP> {
     }
 };
 
+// Both halves of a bf16x2 word mapped at once to their totalOrder keys
+// (per half: a negative value complemented, any other with its top bit set,
+// as key32 does for fp32), so that unsigned 16-bit order is totalOrder, and
+// back.
+__device__ __forceinline__ uint32_t keys16x2(uint32_t w) {
+    const uint32_t neg = ((w >> 15) & 0x00010001u) * 0xFFFFu;  // 0xFFFF in each negative half
+    return w ^ (neg | 0x80008000u);
+}
+__device__ __forceinline__ uint32_t unkeys16x2(uint32_t k) {
+    const uint32_t neg = ((~k >> 15) & 0x00010001u) * 0x7FFFu;  // halves whose key has the top bit clear
+    return k ^ (neg | 0x80008000u);
+}
+
 template <hc_op_t OP>
 struct WordOp<HC_BFLOAT16, OP> {
     __device__ __forceinline__ static uint32_t f(uint32_t a, uint32_t b) {
@@ -96,16 +106,14 @@ struct WordOp<HC_BFLOAT16, OP> {
             return pack_bf16x2(__fadd_rn(bf_lo(a), bf_lo(b)), __fadd_rn(bf_hi(a), bf_hi(b)));
         if (OP == HC_PROD)
             return pack_bf16x2(__fmul_rn(bf_lo(a), bf_lo(b)), __fmul_rn(bf_hi(a), bf_hi(b)));
-        uint32_t alo = a & 0xFFFFu, blo = b & 0xFFFFu, ahi = a >> 16, bhi = b >> 16;
-        uint32_t lo, hi;
-        if (OP == HC_MAX) {
-            lo = key16(alo) < key16(blo) ? blo : alo;
-            hi = key16(ahi) < key16(bhi) ? bhi : ahi;
-        } else {
-            lo = key16(blo) < key16(alo) ? blo : alo;
-            hi = key16(bhi) < key16(ahi) ? bhi : ahi;
-        }
-        return lo | (hi << 16);
+        // max / min by totalOrder, both halves in one SIMD instruction on
+        // their keys; the key map is a bijection, so equal keys are equal
+        // values and the result is the same word whichever operand wins
+        const uint32_t ka = keys16x2(a), kb = keys16x2(b);
+        uint32_t k;
+        if (OP == HC_MAX) asm("max.u16x2 %0, %1, %2;" : "=r"(k) : "r"(ka), "r"(kb));
+        else asm("min.u16x2 %0, %1, %2;" : "=r"(k) : "r"(ka), "r"(kb));
+        return unkeys16x2(k);
     }
 };
 
