@@ -693,3 +693,23 @@ def test_hc_log_reports_the_pipeline_loops():
     quiet = subprocess.run([sys.executable, "-c", HC_LOG_PROGRAM % root], env=env,
                            capture_output=True, text=True, timeout=120)
     assert "hc: " not in quiet.stderr
+
+
+def test_pipeline_allgather_sends_of_one_block_are_one_item():
+    """At each Pipeline AllGather step a rank sends the block it received to
+    the same local rank of the next server and to the other ranks of its own
+    server (the Pipeline article's AllGather timing): the exported plan does
+    both with one record per (rank, block), which reads the block once and
+    writes it to those 8 ranks of a 4 x 8 layout (7 on the last step, which
+    forwards nothing)."""
+    P, pin, n = 32, 8, 8 * 4096
+    pout = P // pin
+    recs, launches = B.hc_step_plan("pipeline", "allgather", P, n, "float32", pin, 0, in_place=True)
+    assert launches == pout
+    for r in recs:
+        (src,) = r["in_ranks"]
+        s, l = divmod(src, pin)
+        local = {s * pin + j for j in range(pin) if j != l}
+        forward = {((s + 1) % pout) * pin + l}
+        want = local | forward if r["launch"] < pout - 1 else local
+        assert set(r["out_ranks"]) == want and len(r["out_ranks"]) == len(want), r
