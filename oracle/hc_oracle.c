@@ -41,8 +41,8 @@
  * in the order the messages are listed.  With loops, every message of loop i
  * covers only the i-th slice of its segment; loops run one after another.
  *
- * Arithmetic, per element and per step (fixed by the spec text and the
- * ring pseudo-code's element-wise reduce_op):
+ * Arithmetic, per element and per step (the ring pseudo-code's element-wise
+ * reduce_op; bf16 kept in bf16 between steps, so every step rounds):
  *   int32 : sum and prod wrap modulo 2^32; max/min by signed compare.
  *   fp32  : IEEE binary32, round to nearest even, no FMA, no flush to zero.
  *   bf16  : widen both operands to binary32, apply the op there, round the
