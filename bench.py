@@ -456,9 +456,10 @@ def config_sweep(args, dev):
 def latency_sweep(B, dev, reps=100):
     """Per-call microseconds of small in-place AllReduces (hot L2): `eager`
     is back-to-back calls from Python (host and device overlap, so the
-    slower of the two decides), `queued` the same calls enqueued behind a
-    spin kernel (the device's own time per call), `graph` one CUDA graph of
-    `reps` calls (graph mode) launched once."""
+    slower of the two decides), `eager_bound` the same with the arguments
+    converted once (_binding.bind_allreduce), `queued` the same calls
+    enqueued behind a spin kernel (the device's own time per call), `graph`
+    one CUDA graph of `reps` calls (graph mode) launched once."""
     import math
     import torch
     stream = torch.cuda.current_stream(dev)
@@ -492,6 +493,16 @@ def latency_sweep(B, dev, reps=100):
             e1.record(stream)
             torch.cuda.synchronize()
             line[mode + "_eager_us"] = round(e0.elapsed_time(e1) / reps * 1e3, 2)
+            # the same from Python with the arguments converted once
+            bound = B.bind_allreduce(ptrs, ptrs, P, n, dt, "sum", algo, opts, sh)
+            bound()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                bound()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            line[mode + "_eager_bound_us"] = round(e0.elapsed_time(e1) / reps * 1e3, 2)
             hold_device(reps)
             e0.record(stream)
             for _ in range(reps):

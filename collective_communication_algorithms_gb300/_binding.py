@@ -207,6 +207,57 @@ def hc_reduce_scatter(send, recv, P, count, dtype, op, algo, opts=None, stream=0
     _check(st, "hc_reduce_scatter")
 
 
+class BoundCall:
+    """One collective call whose arguments were converted to C types once:
+    calling it issues the C entry point again with exactly those arguments
+    (same buffers, sizes, options and stream).  For callers that repeat a
+    call, e.g. once per training step, this skips the per-call argument
+    conversion of the hc_* functions; the status is checked as they do."""
+
+    __slots__ = ("fn", "args", "name", "keep")
+
+    def __init__(self, name, args, keep):
+        self.fn = lib()[name]  # a function object of its own, without argument conversion
+        self.fn.restype = ctypes.c_int
+        self.args = args
+        self.name = name
+        self.keep = keep  # the objects the arguments point into
+
+    def __call__(self):
+        st = self.fn(*self.args)
+        if st:
+            raise HcError(st, self.name)
+
+
+def _bound_args(send, recv, P, count, dtype, opts, stream):
+    sp, rp = _ptr_array(list(send)) if send is not None else None, _ptr_array(list(recv))
+    head = (sp, rp, ctypes.c_int(int(P)), ctypes.c_size_t(int(count)),
+            ctypes.c_int(_enum(DTYPES, dtype)))
+    tail = (ctypes.byref(opts) if opts is not None else None,
+            ctypes.c_void_p(int(stream)) if stream else None)
+    return head, tail, (sp, rp, opts)
+
+
+def bind_allreduce(send, recv, P, count, dtype, op, algo, opts=None, stream=0):
+    """hc_allreduce with these arguments, as a BoundCall."""
+    head, tail, keep = _bound_args(send, recv, P, count, dtype, opts, stream)
+    mid = (ctypes.c_int(_enum(OPS, op)), ctypes.c_int(_enum(ALGOS, algo)))
+    return BoundCall("hc_allreduce", head + mid + tail, keep)
+
+
+def bind_reduce_scatter(send, recv, P, count, dtype, op, algo, opts=None, stream=0):
+    """hc_reduce_scatter with these arguments, as a BoundCall."""
+    head, tail, keep = _bound_args(send, recv, P, count, dtype, opts, stream)
+    mid = (ctypes.c_int(_enum(OPS, op)), ctypes.c_int(_enum(ALGOS, algo)))
+    return BoundCall("hc_reduce_scatter", head + mid + tail, keep)
+
+
+def bind_allgather(send, recv, P, count, dtype, algo, opts=None, stream=0):
+    """hc_allgather with these arguments, as a BoundCall."""
+    head, tail, keep = _bound_args(send, recv, P, count, dtype, opts, stream)
+    return BoundCall("hc_allgather", head + (ctypes.c_int(_enum(ALGOS, algo)),) + tail, keep)
+
+
 def hc_reduce_scatter_static_scratch(send, recv, P, count, dtype, op, algo, ranks_per_server=1,
                                      max_loop_bytes=0, stream=0):
     """Step-mode ReduceScatter whose working memory is the library's own

@@ -369,3 +369,26 @@ def test_zz_no_device_timeouts_recorded():
     """No bounded device-side wait gave up during the GPU tests above."""
     from collective_communication_algorithms_gb300 import _binding as B
     assert B.hc_device_status(clear=False) == 0
+
+
+def test_bound_calls_equal_plain_calls():
+    """BoundCall objects (arguments converted once, the call repeated) give
+    bit for bit what the plain entry points give, call after call."""
+    from collective_communication_algorithms_gb300 import _binding as B
+    P, n = 8, 40000
+    X = hc_inputs.gradients_f32(P, n, seed=77)
+    dev = torch.from_numpy(X).cuda()
+    stream = torch.cuda.current_stream().cuda_stream
+    for algo, mode in (("ring", "fused"), ("rhd", "step"), ("pipeline", "step")):
+        opts = B.make_opts(mode, ranks_per_server=4 if algo == "pipeline" else 1)
+        a, b = torch.zeros_like(dev), torch.zeros_like(dev)
+        rows = lambda t: [t[r].data_ptr() for r in range(P)]
+        B.hc_allreduce(rows(dev), rows(a), P, n, "float32", "sum", algo, opts, stream)
+        call = B.bind_allreduce(rows(dev), rows(b), P, n, "float32", "sum", algo, opts, stream)
+        for _ in range(3):
+            b.zero_()
+            call()
+            torch.cuda.synchronize()
+            assert torch.equal(a.view(torch.int32), b.view(torch.int32)), (algo, mode)
+    assert B.hc_device_status() == 0
+

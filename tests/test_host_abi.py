@@ -713,3 +713,18 @@ def test_pipeline_allgather_sends_of_one_block_are_one_item():
         forward = {((s + 1) % pout) * pin + l}
         want = local | forward if r["launch"] < pout - 1 else local
         assert set(r["out_ranks"]) == want and len(r["out_ranks"]) == len(want), r
+
+
+@host_only
+def test_bound_calls_validate_like_the_entry_points():
+    """A BoundCall (arguments converted once) reports exactly the status the
+    plain entry point reports for the same arguments."""
+    P, n = 8, 4096
+    s, r = fake(P), fake(P, base=BASE + 64 * MB)
+    cases = [(B.bind_allreduce, B.hc_allreduce, (s, r, P, n, "float32", "sum", "ring")),
+             (B.bind_allreduce, B.hc_allreduce, (s, r, 0, n, "float32", "sum", "ring")),
+             (B.bind_allreduce, B.hc_allreduce, ([x + 4 for x in s], r, P, n, "float32", "sum", "rhd")),
+             (B.bind_reduce_scatter, B.hc_reduce_scatter, (s, r, P, n, "bfloat16", "max", "rhd")),
+             (B.bind_allgather, B.hc_allgather, (s, r, P, n, "int32", "ring"))]
+    for bind, plain, args in cases:
+        assert status_of(bind(*args)) == status_of(plain, *args), (bind.__name__, args[2])
