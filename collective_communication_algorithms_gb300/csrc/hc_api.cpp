@@ -547,9 +547,12 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
     // Constants measured on GB300 (a C caller; bench.py --sweep select, the
     // benchmark's configurations and a C timing loop around the entry points):
     //  host: 0.55 us of the library's own work per call, 1.4 us per launch;
-    //  step mode: 2.8 us of device time per dependent launch, and the
-    //    fraction of the copy bandwidth each schedule's steps reach on their
-    //    own bytes (Ring above 1: its partial sums come back from L2);
+    //  step mode: the device time per dependent launch of each schedule
+    //    (Ring 1.9 us; RHD 2.6 us below 16 ranks and 4.5 us from 16, whose
+    //    launches carry many items with scattered block sets; Pipeline 2.4 us;
+    //    hierarchical 3.1 us, fewer but heavier launches), and the fraction of
+    //    the copy bandwidth each schedule's steps reach on their own bytes
+    //    (above 1 where the steps' partial sums come back from L2);
     //  fused mode: a fixed device cost per call that grows with the ranks a
     //    block reduces (1.55 us + per-rank cost of the schedule's reduction:
     //    the Ring chain, the RHD tree -- compile-time below 16 ranks, looped
@@ -557,7 +560,7 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
     //    AllGather's plain copies), then the bytes at the path's fraction of
     //    the bandwidth (AllReduce / ReduceScatter TMA-staged up to 32 ranks;
     //    AllGather register path below 16 ranks, TMA-staged above).
-    const double kHostCallUs = 0.55, kHostLaunchUs = 1.4, kStepLaunchUs = 2.8;
+    const double kHostCallUs = 0.55, kHostLaunchUs = 1.4;
     const double kFusedBaseUs = 1.55, kBandwidth = 6800e9;
     if (!out_algo || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
     if (mode != HC_MODE_FUSED && mode != HC_MODE_STEP) return HC_ERR_INVALID_ARG;
@@ -578,9 +581,16 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
         if (hc_schedule_stats(a, coll, P, rps, count, dtype, 0, &st, nullptr) != HC_OK) continue;
         double host, dev;
         if (mode == HC_MODE_STEP) {
-            const double f = a == HC_ALGO_RING ? 1.1 : a == HC_ALGO_RHD ? 1.0 : 0.96;
+            const double launch_us = a == HC_ALGO_RING       ? 1.9
+                                     : a == HC_ALGO_RHD      ? (P < 16 ? 2.6 : 4.5)
+                                     : a == HC_ALGO_PIPELINE ? 2.4
+                                                             : 3.1;
+            const double f = a == HC_ALGO_RING       ? 1.1
+                             : a == HC_ALGO_RHD      ? 1.0
+                             : a == HC_ALGO_PIPELINE ? 1.1
+                                                     : 1.12;
             host = kHostCallUs + st.launches_step * kHostLaunchUs;
-            dev = st.launches_step * kStepLaunchUs + (double)st.step_bytes / (f * kBandwidth) * 1e6;
+            dev = st.launches_step * launch_us + (double)st.step_bytes / (f * kBandwidth) * 1e6;
         } else {
             double per_rank, f;
             if (copy) {

@@ -392,12 +392,14 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
  * hides under the memory traffic).  Launches are queued asynchronously, so
  * the host's launch cost and the device time overlap:
  *   t = max(c_host + launches * alpha_host, t_device)
- *   step:  t_device = launches * alpha_step + step_bytes / (f_algo * B)
+ *   step:  t_device = launches * alpha_algo + step_bytes / (f_algo * B)
  *   fused: t_device = alpha_fused + r_algo * P + fused_bytes / (f_path * B)
  * with launches and bytes from hc_schedule_stats and, measured on GB300 for
- * a C caller: c_host = 0.55 us, alpha_host = 1.4 us per launch,
- * alpha_step = 2.8 us per dependent launch, f_algo = 1.1 (Ring: its partial
- * sums come back from L2), 1.0 (RHD), 0.96 (Pipeline, hierarchical);
+ * a C caller: c_host = 0.55 us, alpha_host = 1.4 us per launch; alpha_algo
+ * per dependent launch 1.9 us (Ring), 2.6 us (RHD below 16 ranks), 4.5 us
+ * (RHD from 16), 2.4 us (Pipeline), 3.1 us (hierarchical); f_algo = 1.1
+ * (Ring, Pipeline: their partial sums come back from L2), 1.0 (RHD), 1.12
+ * (hierarchical);
  * alpha_fused = 1.55 us, r_algo the per-rank cost of the schedule's
  * reduction in one block (Ring 0.055 us, RHD 0.04 below 16 ranks and 0.067
  * from 16, Pipeline 0.07, hierarchical 0.083, AllGather / Broadcast 0.03),
