@@ -78,8 +78,11 @@ struct DevItem {
                        // ranks' own inputs), so they may be loaded before the
                        // wait on the previous launch (see StepParams::early)
     int16_t seg_width, seg_reps;
-    int16_t once;      // 1: no other item of the launch reads this item's inputs or
+    uint8_t once;      // 1: no other item of the launch reads this item's inputs or
                        // accumulator, so its loads may leave L2 first
+    uint8_t keep;      // bit 0 / bit 1: a later launch of the call reads the block
+                       // written to the first / second output set; the other
+                       // outputs are final and their stores may leave L2 first
     int32_t seg_first, seg_stride;
     int32_t cta_begin;  // first CTA of this item in the launch grid
     int16_t out2_base, out2_rot, out2_mod, out2_cnt;

@@ -52,18 +52,19 @@ constexpr int kStepBatch = 8;  // input loads in flight per vector
 // 0.83 with one, and the hierarchical steps 0.91 against 0.87.
 constexpr int kStepUnroll = 2;
 
-// Calls f(rank) for every output of an item: its output set, then its
-// second output set (a merged copy of the same block).
+// Calls f(rank, kept) for every output of an item: its output set, then its
+// second output set (a merged copy of the same block).  `kept`: a later step
+// of the call reads that set's block (DevItem::keep).
 template <class F>
 __device__ __forceinline__ void each_output(const DevItem& I, F f) {
     int o = I.out_rot;
     for (int j = 0; j < I.out_cnt; j++) {
-        f(I.out_base + o);
+        f(I.out_base + o, (I.keep & 1) != 0);
         if (++o == I.out_mod) o = 0;
     }
     o = I.out2_rot;
     for (int j = 0; j < I.out2_cnt; j++) {
-        f(I.out2_base + o);
+        f(I.out2_base + o, (I.keep & 2) != 0);
         if (++o == I.out2_mod) o = 0;
     }
 }
@@ -89,7 +90,10 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
     // read again (this step's outputs).  On GB300 this took the Ring
     // AllReduce fp32 step mode from 0.94 to 1.15 of the copy bandwidth on its
     // own bytes (the accumulators then come from L2), the Ring
-    // ReduceScatter / AllGather steps from 0.84 / 0.85 to 0.99.
+    // ReduceScatter / AllGather steps from 0.84 / 0.85 to 0.99.  Outputs no
+    // later step reads (the results of the last steps) are stored with the
+    // same policy: Ring AllGather step mode 1.11 -> 1.15, bf16 AllReduce
+    // steps 0.916 -> 0.926.
     const uint64_t first_out = l2_evict_first_policy();
     auto ld_vec = [&](uintptr_t a) -> uint4 { return I.once ? ld_vec_hint(a, first_out) : hc::ld_vec(a); };
     // Programmatic dependent launch: this grid may be scheduled while the
@@ -126,10 +130,15 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
 #pragma unroll
                     for (int u = 0; u < kStepUnroll; u++) x[u] = vop<DT, OP>(a[u], x[u]);
                 }
-                each_output(I, [&](int r) {
+                each_output(I, [&](int r, bool kept) {
                     const uintptr_t ob = p.base[I.out_loc][r];
+                    if (kept) {
 #pragma unroll
-                    for (int u = 0; u < kStepUnroll; u++) st_vec(ob + o[u], x[u]);
+                        for (int u = 0; u < kStepUnroll; u++) st_vec(ob + o[u], x[u]);
+                    } else {
+#pragma unroll
+                        for (int u = 0; u < kStepUnroll; u++) st_vec_hint(ob + o[u], x[u], first_out);
+                    }
                 });
                 e += (kStepUnroll - 1) * nthreads * A;  // the loop step adds the last stride
                 continue;
@@ -157,7 +166,10 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
                         if (q < m) v = (c == 0 && q == 0) ? x[0] : vop<DT, OP>(v, x[q]);
                 }
                 if (I.acc_rank >= 0) v = vop<DT, OP>(acc, v);
-                each_output(I, [&](int r) { st_vec(p.base[I.out_loc][r] + off, v); });
+                each_output(I, [&](int r, bool kept) {
+                    if (kept) st_vec(p.base[I.out_loc][r] + off, v);
+                    else st_vec_hint(p.base[I.out_loc][r] + off, v, first_out);
+                });
             } else {
                 // ragged end of the rank vector: element by element
                 for (int64_t x = e; x < hi; x++) {
@@ -170,7 +182,7 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
                     }
                     if (I.acc_rank >= 0)
                         v = vop<DT, OP>(ld_elem<ES>(p.base[I.acc_loc][I.acc_rank] + xo), v);
-                    each_output(I, [&](int r) { st_elem<ES>(p.base[I.out_loc][r] + xo, v); });
+                    each_output(I, [&](int r, bool) { st_elem<ES>(p.base[I.out_loc][r] + xo, v); });
                 }
             }
         }
@@ -223,9 +235,11 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
     // else (the accumulator, every store) comes after it.
     const bool early = staged && p.early && I.early;
     // L2 policies as in step_kernel: operands read by this item only leave
-    // L2 first; the outputs, which the next step reads, leave it last (on
-    // GB300 the Pipeline 4 x 8 step mode went from 0.82 to 0.86 of the copy
-    // bandwidth on its own bytes, the hierarchical from 0.92 to 0.94)
+    // L2 first; outputs a later step reads leave it last (on GB300 the
+    // Pipeline 4 x 8 step mode went from 0.82 to 0.86 of the copy bandwidth
+    // on its own bytes, the hierarchical from 0.92 to 0.94), outputs nobody
+    // reads again leave it first (Pipeline 4 x 8 AllReduce / AllGather step
+    // mode 0.92 / 0.88 -> 0.95 / 0.93, hierarchical 1.03 -> 1.05)
     const uint64_t first_out = l2_evict_first_policy();
     auto load = [&](int slot, uintptr_t src) {
         if (I.once) bulk_g2s_hint(smem + (size_t)slot * kTmaTile, src, tb, full, first_out);
@@ -263,7 +277,9 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
             // bulk stores; the block leaves once they have read it
             if (threadIdx.x == 0) {
                 const uint64_t last_out = l2_evict_last_policy();
-                each_output(I, [&](int r) { bulk_s2g_hint(p.base[I.out_loc][r] + off, smem, tb, last_out); });
+                each_output(I, [&](int r, bool kept) {
+                    bulk_s2g_hint(p.base[I.out_loc][r] + off, smem, tb, kept ? last_out : first_out);
+                });
                 bulk_commit();
                 bulk_wait_read_all();
             }
@@ -273,7 +289,9 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
                 v = vop<DT, OP>(v, *(const uint4*)(smem + (size_t)j * kTmaTile + vo));
             if (acc_slot >= 0) v = vop<DT, OP>(*(const uint4*)(smem + (size_t)acc_slot * kTmaTile + vo), v);
             const uint64_t last_out = l2_evict_last_policy();
-            each_output(I, [&](int r) { st_vec_hint(p.base[I.out_loc][r] + off + vo, v, last_out); });
+            each_output(I, [&](int r, bool kept) {
+                st_vec_hint(p.base[I.out_loc][r] + off + vo, v, kept ? last_out : first_out);
+            });
         }
     }
     if (tile == 0 && threadIdx.x == 0) {
@@ -287,7 +305,7 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
                 v = vop<DT, OP>(v, ld_elem<ES>(p.base[I.in_loc][I.in_base + rr] + xo));
             }
             if (acc_slot >= 0) v = vop<DT, OP>(ld_elem<ES>(p.base[I.acc_loc][I.acc_rank] + xo), v);
-            each_output(I, [&](int r) { st_elem<ES>(p.base[I.out_loc][r] + xo, v); });
+            each_output(I, [&](int r, bool) { st_elem<ES>(p.base[I.out_loc][r] + xo, v); });
         }
     }
 }

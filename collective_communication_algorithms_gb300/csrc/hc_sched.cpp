@@ -30,6 +30,7 @@
 #include <algorithm>
 #include <cstring>
 #include <map>
+#include <set>
 #include <tuple>
 
 #include "hc_internal.h"
@@ -700,6 +701,42 @@ bool build_plan(hc_algo_t algo, hc_coll_t coll, int P, int p_intra, int root, in
     };
     for (auto& items : bound) mark_once(items);
     mark_once(final_items);
+
+    // outputs a later launch of the call reads: within a loop, a later step
+    // or the final moves (each loop acts on its own slice, so only the steps
+    // after this one in the same loop see its output); an in-place rank's
+    // original buffer is its working buffer, and so is an in-place
+    // ReduceScatter's output segment
+    auto canon = [&](int loc, int q, int k) {
+        if ((loc == LOC_ORIG && alias.orig_is_work[q]) || (loc == LOC_FINAL && alias.final_is_work[q]))
+            loc = LOC_WORK;
+        return std::make_tuple(loc, q, k);
+    };
+    std::set<std::tuple<int, int, int>> read_later;
+    auto note_reads = [&](const std::vector<DevItem>& items) {
+        for (const DevItem& it : items)
+            for (int i = 0; i < it.seg_width * it.seg_reps; i++) {
+                const int k = it.seg_first + (i / it.seg_width) * it.seg_stride + i % it.seg_width;
+                for (int j = 0; j < it.in_cnt; j++)
+                    read_later.insert(canon(it.in_loc, it.in_base + (it.in_rot + j) % it.in_mod, k));
+                if (it.acc_rank >= 0) read_later.insert(canon(it.acc_loc, it.acc_rank, k));
+            }
+    };
+    auto set_read_later = [&](const DevItem& it, int base, int rot, int mod, int cnt) {
+        for (int i = 0; i < it.seg_width * it.seg_reps; i++) {
+            const int k = it.seg_first + (i / it.seg_width) * it.seg_stride + i % it.seg_width;
+            for (int j = 0; j < cnt; j++)
+                if (read_later.count(canon(it.out_loc, base + (rot + j) % mod, k))) return true;
+        }
+        return false;
+    };
+    note_reads(final_items);  // the final moves' outputs are read by nobody
+    for (size_t si = bound.size(); si-- > 0;) {
+        for (DevItem& it : bound[si])
+            it.keep = (uint8_t)((set_read_later(it, it.out_base, it.out_rot, it.out_mod, it.out_cnt) ? 1 : 0) |
+                                (set_read_later(it, it.out2_base, it.out2_rot, it.out2_mod, it.out2_cnt) ? 2 : 0));
+        note_reads(bound[si]);
+    }
 
     if (plan.lay.n == 0) return true;
     for (int lp = 0; lp < plan.sl.loops; lp++) {
