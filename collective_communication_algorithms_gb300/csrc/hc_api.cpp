@@ -548,7 +548,7 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
     // benchmark's configurations and a C timing loop around the entry points):
     //  host: 0.55 us of the library's own work per call, 1.4 us per launch;
     //  step mode: the device time per dependent launch of each schedule
-    //    (Ring 1.9 us; RHD 2.6 us below 16 ranks and 4.5 us from 16, whose
+    //    (Ring 1.9 us; RHD 2.2 us below 16 ranks and 2.6 us from 16, whose
     //    launches carry many items with scattered block sets; Pipeline 2.4 us;
     //    hierarchical 3.1 us, fewer but heavier launches), and the fraction of
     //    the copy bandwidth each schedule's steps reach on their own bytes
@@ -558,8 +558,9 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
     //    the Ring chain, the RHD tree -- compile-time below 16 ranks, looped
     //    above --, the Pipeline and hierarchical two-level trees, the
     //    AllGather's plain copies), then the bytes at the path's fraction of
-    //    the bandwidth (AllReduce / ReduceScatter TMA-staged up to 32 ranks;
-    //    AllGather register path below 16 ranks, TMA-staged above).
+    //    the bandwidth (AllReduce / ReduceScatter TMA-staged up to 32 ranks,
+    //    register path above; the AllGather's plain copies, whose writes per
+    //    byte read grow with the ranks).
     const double kHostCallUs = 0.55, kHostLaunchUs = 1.4;
     const double kFusedBaseUs = 1.55, kBandwidth = 6800e9;
     if (!out_algo || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
@@ -582,7 +583,7 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
         double host, dev;
         if (mode == HC_MODE_STEP) {
             const double launch_us = a == HC_ALGO_RING       ? 1.9
-                                     : a == HC_ALGO_RHD      ? (P < 16 ? 2.6 : 4.5)
+                                     : a == HC_ALGO_RHD      ? (P < 16 ? 2.2 : 2.6)
                                      : a == HC_ALGO_PIPELINE ? 2.4
                                                              : 3.1;
             const double f = a == HC_ALGO_RING       ? 1.1

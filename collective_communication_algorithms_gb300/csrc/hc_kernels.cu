@@ -82,9 +82,34 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
     while (it + 1 < p.nitems && p.items[it + 1].cta_begin <= b) it++;
     const DevItem& I = p.items[it];
     const int cend = (it + 1 < p.nitems) ? p.items[it + 1].cta_begin : p.total_ctas;
-    const int64_t nthreads = (int64_t)(cend - I.cta_begin) * blockDim.x;
-    const int64_t t0 = (int64_t)(b - I.cta_begin) * blockDim.x + threadIdx.x;
+    const int ncta = cend - I.cta_begin;
+    const int bl = b - I.cta_begin;
     const int nseg = I.seg_width * I.seg_reps;
+    // An item that spans several segments gives each segment its own blocks
+    // (ncta / nseg of them; the host assigns at least one per segment), and
+    // each segment's blocks stride over its slice.  (All of an item's threads
+    // striding over one segment after another left those past a segment's
+    // vector count idle and made the others visit every segment in turn: RHD
+    // steps, whose items span up to P / 2 segments, paid that latency per
+    // segment.)  With fewer blocks than segments a block takes every
+    // ncta-th segment.
+    int si_begin = 0, si_step = 1, cps = ncta, cb = bl;  // cb: block within its segment's
+    if (nseg > 1) {
+        if (ncta >= nseg) {
+            cps = ncta / nseg;
+            si_begin = bl / cps;
+            si_step = nseg;
+            if (si_begin >= nseg) return;  // the remainder of the division
+            cb = bl - si_begin * cps;
+        } else {
+            cps = 1;
+            si_begin = bl;
+            si_step = ncta;
+            cb = 0;
+        }
+    }
+    const int64_t nthreads = (int64_t)cps * blockDim.x;
+    const int64_t t0 = (int64_t)cb * blockDim.x + threadIdx.x;
     // Operands no other item of this launch reads are loaded with an L2
     // evict-first policy, so that what stays in L2 is what the next steps
     // read again (this step's outputs).  On GB300 this took the Ring
@@ -103,7 +128,7 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
-    for (int si = 0; si < nseg; si++) {
+    for (int si = si_begin; si < nseg; si += si_step) {
         const int seg = I.seg_first + (si / I.seg_width) * I.seg_stride + (si % I.seg_width);
         const int64_t sbeg = (int64_t)seg * p.L;
         int64_t send_ = sbeg + p.L;
@@ -343,75 +368,9 @@ fused_allgather(const __grid_constant__ FusedParams p) {
     }
 }
 
-// ---------------------------------------------------------------------------
-// TMA-staged AllGather.  One elected thread moves a 16-byte-aligned tile
-// between HBM and shared memory with the bulk-copy engine (cp.async.bulk),
-// completion tracked by an mbarrier transaction count, and bulk-stores it from
-// shared memory to all outputs.  Every wait on the mbarrier is bounded: after
-// p.wait_ns the block records HC_ERR_TIMEOUT in hc_device_error, waits
-// (again bounded) for its copy in flight and returns without storing; in the
-// wait-expiry test mode (p.hold) the first wait expires by construction, as
-// in fused_reduce_tma.
-// ---------------------------------------------------------------------------
-// One 32 KB tile per block, a block for every tile of every segment: blocks
-// are scheduled in index order, so the stores sweep each output from its
-// start.  On GB300 this beat one persistent block per SM streaming its tiles
-// through 6 stages (the previous design) by 9 % at P = 8 and 8 % at P = 32
-// (AllGather fp32, out of place), and up to 7 blocks share an SM.
-constexpr int kAgTile = 32768;          // bytes per block
+// Library error flag of the kernels' bounded waits (HC_ERR_TIMEOUT), read and
+// cleared by hc_device_status.
 __device__ int hc_device_error;
-
-// AllGather, TMA-staged: block (t, seg) loads tile t of the owner's segment
-// into shared memory once and bulk-stores it to every rank (the owner's own
-// copy only when it is not already in place).  Broadcast: one segment owned
-// by the root.
-template <int ES>
-__global__ void __launch_bounds__(32)
-fused_allgather_tma(const __grid_constant__ FusedParams p) {
-    constexpr int A = 16 / ES;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int seg = blockIdx.y;
-    const int k = p.owner >= 0 ? p.owner : seg;
-    const int64_t sbeg = (int64_t)seg * p.L;
-    const int64_t send_ = sbeg + p.L < p.n ? sbeg + p.L : p.n;
-    const int64_t nfull = send_ > sbeg ? (send_ - sbeg) / A : 0;
-    const bool skip_own = (p.skip_mask >> k) & 1ull;
-    asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (threadIdx.x != 0) return;
-    uint64_t* full = (uint64_t*)(smem + kAgTile);
-    const int64_t nbytes = nfull * 16;
-    const int64_t t0 = (int64_t)blockIdx.x * kAgTile;
-    if (t0 < nbytes) {
-        const int64_t left = nbytes - t0;
-        const unsigned tb = (unsigned)(left < kAgTile ? left : kAgTile);
-        const uintptr_t off = (uintptr_t)sbeg * ES + (uintptr_t)t0;
-        mbar_init(full, 1 + p.hold);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-        mbar_arrive_expect_tx(full, tb);
-        bulk_g2s(smem, p.src[k] + off, tb, full);
-        if (!mbar_wait_bounded(full, 0, p.wait_ns)) {
-            mbar_expired(full, p.err, p.hold, true);
-            return;
-        }
-        // each output line is written once and not read again here: let
-        // it leave L2 first (on GB300, P = 32: 156 against 160 us)
-        const uint64_t pol = l2_evict_first_policy();
-        for (int r = 0; r < p.P; r++)
-            if (r != k || !skip_own) bulk_s2g_hint(p.dst[r] + off, smem, tb, pol);
-        bulk_commit();
-        bulk_wait_all();
-    }
-    if (blockIdx.x == 0) {
-        // ragged end of the segment (< 16 bytes)
-        for (int64_t x = sbeg + nfull * A; x < send_; x++) {
-            const uintptr_t xo = (uintptr_t)x * ES;
-            const uint32_t val = ld_elem<ES>(p.src[k] + xo);
-            for (int r = 0; r < p.P; r++)
-                if (r != k || !skip_own) st_elem<ES>(p.dst[r] + xo, val);
-        }
-    }
-}
 
 // ---------------------------------------------------------------------------
 // dispatch
@@ -707,23 +666,17 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
     // 6.3 TB/s.  Buffers in page-locked host memory keep a persistent grid
     // (the host link, not HBM, bounds them).
     if (a.coll == HC_COLL_ALLGATHER || a.coll == HC_COLL_BROADCAST) {
-        // TMA path for 16 or more ranks once every segment holds several
-        // tiles; fewer ranks, and buffers in host memory, take the plain
-        // load / store path.  On GB300 (fp32, out of place, same call): P = 8,
-        // 64 MiB per rank: register path 92.3 - 93.5 us, TMA 95.0 - 96.5 us;
-        // P = 32, 32 MiB per rank: register path 166 us, TMA with
-        // evict-first stores 156 us.  The same store pattern without the
-        // loads takes 73.8 us (P = 8), so the 64 MiB of reads cost about
-        // 19 us of a 92 us call: reads and writes share the DRAM bus.
-        if (a.P >= 16 && seg_bytes >= 16 * (int64_t)kAgTile && !a.host_buffers) {
-            void* fn = es == 2 ? (void*)fused_allgather_tma<2> : (void*)fused_allgather_tma<4>;
-            p.err = device_error_flag();
-            if (!p.err) return cudaErrorInvalidValue;
-            const int smem = kAgTile + 16;
-            if (!allow_smem(fn, smem)) return cudaErrorInvalidValue;
-            const int64_t tiles = (seg_bytes + kAgTile - 1) / kAgTile;
-            return launch_pdl(fn, dim3((unsigned)tiles, S), dim3(32), args, smem, stream);
-        }
+        // The plain load / store path at every rank count.  A TMA-staged
+        // variant (one 32 KB tile per block, bulk-loaded once and
+        // bulk-stored to every rank) measured on GB300 (fp32, out of place,
+        // one call) between 5.0 and 7.2 TB/s on (P + 1) n b depending on the
+        // grid's shape: 20 - 30 % slower than this path at 4 Mi elements per
+        // rank for 16, 32 and 64 ranks (P = 32: 106 against 82 us), 3 - 6 %
+        // faster at 8 Mi, with no layout, tile size or store order that
+        // removed the dips; this path stays at 6.6 - 6.95 TB/s over 8 to 64
+        // ranks and 1 to 32 Mi elements.  The same store pattern without the
+        // loads takes 73.8 us at P = 8, 64 MiB per rank, against 89 - 93 us
+        // with them: reads and writes share the DRAM bus.
         void* fn = es == 2 ? (void*)fused_allgather<2> : (void*)fused_allgather<4>;
         const int64_t vecs = (lay.L + lay.A - 1) / lay.A;
         const int64_t want = std::max<int64_t>(1, (vecs + kFusedThreads - 1) / kFusedThreads);

@@ -799,7 +799,7 @@ static int64_t item_vectors(const DevItem& it, const PlanLaunch& L, const Layout
 // CTAs per item: one per `threads` vectors when the budget allows; otherwise
 // the budget is shared in proportion to the bytes each item moves (vectors x
 // its inputs, accumulator and outputs), so that items of one launch finish
-// together.  (Shared by vectors alone, a Pipeline AllGather step whose 1 -> 7
+// together; and never fewer than the item's segments.  (Shared by vectors alone, a Pipeline AllGather step whose 1 -> 7
 // broadcast items sit beside 1 -> 1 forwards gave both kinds the same CTAs
 // and ran at 0.68 of the copy bandwidth on GB300.)
 int assign_ctas(PlanLaunch& L, const Layout& lay, int threads, int max_ctas) {
@@ -820,6 +820,9 @@ int assign_ctas(PlanLaunch& L, const Layout& lay, int threads, int max_ctas) {
     for (int i = 0; i < ni; i++) {
         int64_t c = need[i];
         if (total > budget) c = std::min(need[i], std::max<int64_t>(1, weight[i] * budget / wsum));
+        // at least one CTA per segment: the step kernel gives each of an
+        // item's segments its own CTAs
+        c = std::max<int64_t>(c, (int64_t)L.items[i].seg_width * L.items[i].seg_reps);
         L.items[i].cta_begin = begin;
         begin += (int)c;
     }

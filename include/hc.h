@@ -396,7 +396,7 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
  *   fused: t_device = alpha_fused + r_algo * P + fused_bytes / (f_path * B)
  * with launches and bytes from hc_schedule_stats and, measured on GB300 for
  * a C caller: c_host = 0.55 us, alpha_host = 1.4 us per launch; alpha_algo
- * per dependent launch 1.9 us (Ring), 2.6 us (RHD below 16 ranks), 4.5 us
+ * per dependent launch 1.9 us (Ring), 2.2 us (RHD below 16 ranks), 2.6 us
  * (RHD from 16), 2.4 us (Pipeline), 3.1 us (hierarchical); f_algo = 1.1
  * (Ring, Pipeline: their partial sums come back from L2), 1.0 (RHD), 1.12
  * (hierarchical);
@@ -404,7 +404,8 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
  * reduction in one block (Ring 0.055 us, RHD 0.04 below 16 ranks and 0.067
  * from 16, Pipeline 0.07, hierarchical 0.083, AllGather / Broadcast 0.03),
  * f_path = 1.0 (AllReduce / ReduceScatter up to 32 ranks, 0.96 above), 0.94
- * (AllGather / Broadcast below 16 ranks) or 1.02 (from 16); B = 6800 GB/s.
+ * (AllGather / Broadcast below 16 ranks) or 1.02 (from 16, where each byte
+ * read is written more often); B = 6800 GB/s.
  * Candidates: Ring and RHD; Pipeline and, for an AllReduce, the
  * hierarchical AllReduce when ranks_per_server > 1 divides P; Broadcast:
  * RHD only.  Between equal costs the lower device time wins, then the
@@ -418,8 +419,10 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
 
 /*
  * Device-side status of the kernels that wait on shared-memory barriers (the
- * TMA-staged fused kernels).  Each such wait gives up after about 2 s; the
- * kernel then records HC_ERR_TIMEOUT here and returns instead of hanging.
+ * TMA-staged kernels: fused AllReduce / ReduceScatter, and the step kernel's
+ * launches of wide reduces and broadcasts).  Each such wait gives up after
+ * about 2 s; the kernel then records HC_ERR_TIMEOUT here and returns instead
+ * of hanging.
  * Returns HC_OK, HC_ERR_TIMEOUT, or HC_ERR_CUDA if the flag cannot be read.
  * Synchronises with the current device (it copies the flag to the host);
  * clear != 0 resets the flag.
@@ -432,7 +435,7 @@ hc_status_t hc_device_status(int clear);
 
 /*
  * Test hook for the path above (no counterpart on the pages).  enable = 1
- * switches every TMA-staged fused kernel launched from then on (any host
+ * switches every TMA-staged kernel launched from then on (any host
  * thread) into a mode in which the copies' shared-memory barrier waits for
  * one arrival more than the block makes before its first wait, and that
  * first wait gives up after 1 ms instead of 2 s.  Every copy still lands;

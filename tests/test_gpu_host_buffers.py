@@ -120,8 +120,8 @@ def check_host(coll, algo, X, dtype, op, mode, p_intra=1, root=0, recv_on_device
 
 
 # 1,100,007 elements of a 4-byte type over 8 ranks put 537 KB in each
-# segment: device buffers of that size take the TMA AllGather path (at least
-# 16 tiles of 32 KB), host buffers must not
+# segment: many blocks per segment on the device path, the persistent grid
+# of the host-buffer path
 SIZES = (37, 4099, 1100007)
 
 

@@ -6,7 +6,7 @@ of the 2^31- and 2^32-byte marks, of every segment edge and of the vector's
 end) are compared with the definition evaluated by the oracle on the same
 sampled columns.  int32 sum and max are exact whatever the association
 order, so every schedule and mode must match bit for bit.  Covers the fused
-register path (AllReduce, ReduceScatter), the TMA AllGather and the step
+register path (AllReduce, ReduceScatter), the AllGather and the step
 kernels (Ring AllReduce)."""
 import numpy as np
 import pytest
@@ -105,7 +105,7 @@ def test_reducescatter_and_allgather_beyond_4GiB(bufs):
     for r, (off, ln) in enumerate(segs):
         m = (J >= off) & (J < off + ln)
         assert np.array_equal(gather(out[r], J[m] - off), want[m]), r
-    # AllGather of the reduced segments (TMA path: each segment is ~1.3 GiB)
+    # AllGather of the reduced segments (each segment is ~1.3 GiB)
     for t in recv:
         t.fill_(0x5A5A5A5A)
     B.hc_allgather([t.data_ptr() for t in out], [t.data_ptr() for t in recv], P, N, "int32", "ring",

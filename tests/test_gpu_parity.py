@@ -310,11 +310,11 @@ def test_fused_around_the_tma_rank_limit(algo, dtype):
 @pytest.mark.parametrize("algo", ALGOS)
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_tma_staged_paths(algo, dtype):
-    """Segments long enough for the TMA-staged AllGather (16 or more ranks and
-    at least 16 tiles of 32 KB per segment; fewer ranks take the register
-    path), with a partial last tile and a ragged end; AllReduce and
-    ReduceScatter at the same sizes (TMA-staged reduce, and the register path
-    where the library picks it: 4- and 2-byte types, sum and max)."""
+    """Segments of many 2 KB tiles of the TMA-staged fused reduce, with a
+    partial last tile and a ragged end, for AllReduce and ReduceScatter
+    (TMA-staged, and the register path where the library picks it: 4- and
+    2-byte types, sum and max); the AllGather at twice the length (the
+    register path at every rank count)."""
     from collective_communication_algorithms_gb300 import _binding as B
     per_seg = 70000 if dtype != "bfloat16" else 135000
     for P in (2, 3, 5, 8, 16, 17):
@@ -337,7 +337,7 @@ def test_broadcast(mode, dtype):
     """RHD Broadcast: every rank ends with the root's vector, bit for bit."""
     for P in (1, 2, 3, 5, 8, 12, 16):
         roots = range(P) if P <= 8 else (0, 1, P // 2, P - 1)
-        # 300,007 elements: the TMA-staged path (at least 16 tiles of 32 KB)
+        # 300,007 elements: many blocks per segment
         for n in (1, 37, 4099, 80000 + 3, 300007):
             X = inputs(dtype, P, n, seed=P * 13 + n, op="sum")
             for root in roots:

@@ -8,8 +8,9 @@ expects one arrival more than the block makes before its first wait, whose
 limit drops to 1 ms, so that wait expires although every copy lands; the
 block then records the timeout, makes the held arrival, waits for its copies
 and exits.  These tests check, for the fused AllReduce / ReduceScatter
-(fused_reduce_tma), the fused AllGather (fused_allgather_tma) and the
-step-mode mesh reduce (step_kernel_tma), that
+(fused_reduce_tma) and the TMA-staged step kernel (step_kernel_tma: the
+Pipeline's mesh reduce, and its AllGather steps' broadcasts by bulk
+stores), that
 
   * the call completes, well inside the 2 s normal limit (no second wait
     ran out: the held arrival released the barrier),
@@ -45,14 +46,14 @@ from gpu_util import expected, run_collective, same_bits, segments  # noqa: E402
 HC_OK, HC_ERR_TIMEOUT = 0, 6
 
 # (collective, algo, mode, P, n, ranks_per_server): each case runs a
-# TMA-staged kernel -- the AllGather has 16 ranks and segments of at least
-# 16 tiles of 32 KB, the step-mode Pipeline starts with a mesh reduce of 4
-# inputs
+# TMA-staged kernel -- the step-mode Pipeline AllReduce starts with a mesh
+# reduce of 4 inputs, and every launch of the step-mode Pipeline AllGather
+# (2 servers of 4) copies each block to 4 ranks by bulk stores
 CASES = [
     ("allreduce", "ring", "fused", 8, 40003, 1),
     ("reducescatter", "rhd", "fused", 12, 30011, 1),
-    ("allgather", "ring", "fused", 16, 16 * 131072 + 40, 1),
     ("allreduce", "pipeline", "step", 8, 20011, 4),
+    ("allgather", "pipeline", "step", 8, 8 * 20011 + 5, 4),
 ]
 
 
