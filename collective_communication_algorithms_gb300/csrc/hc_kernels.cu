@@ -217,18 +217,30 @@ step_kernel(const __grid_constant__ StepParams<MAXI> p) {
 // Step kernel, TMA-staged: for launches whose items combine three or more
 // operands (the intra-server mesh reduce of the Pipeline and of the
 // hierarchical AllReduce: up to p_intra inputs plus the partial that arrived
-// on the inter-server ring).  Block (item, segment, tile) bulk-copies tile
-// `tile` (kTmaTile bytes) of the launch's slice of that segment from every
+// on the inter-server ring), launches of pure broadcasts, and large launches
+// of narrow items (below).  Block (item, segment, tile) bulk-copies tile
+// `tile` (TILE bytes) of the launch's slice of that segment from every
 // operand -- the item's inputs in their order, then its accumulator -- into
-// consecutive kTmaTile slots of shared memory, all completing on one
-// mbarrier.  Each thread then combines its 16-byte vector exactly as
-// step_kernel does (in[0] (+) in[1] (+) ..., then acc (+) that) and stores it
-// to every output.  The mbarrier waits are bounded like fused_reduce_tma's.
-// On GB300 the register path (BATCH = 8, 4 blocks per SM) ran these
-// launches at 0.79 of the copy bandwidth.
+// consecutive TILE-byte slots of shared memory, all completing on one
+// mbarrier.  The threads then combine its 16-byte vectors exactly as
+// step_kernel does (in[0] (+) in[1] (+) ..., then acc (+) that) and store
+// them to every output.  The mbarrier waits are bounded like
+// fused_reduce_tma's.  On GB300 the register path (BATCH = 8, 4 blocks per
+// SM) ran the wide launches at 0.79 of the copy bandwidth.
 constexpr int kStepTmaMaxOperands = kTmaMaxRanks;  // shared memory <= 64 KB per block
+// Narrow launches (items of at most two operands: the Ring and RHD steps,
+// the inter-server steps) take this kernel too once a launch moves at least
+// kNarrowTmaMinBytes, with 8 KB tiles: on GB300 the Ring AllReduce fp32 step
+// mode went from 1.17 to 1.30 of the copy bandwidth on its own bytes, the
+// Ring AllGather steps from 1.15 to 1.31, the bf16 Ring / RHD AllReduce
+// steps (128 MiB per rank) from 0.93 to 1.04 / 1.06.  With 2 KB tiles they
+// ran at 0.5 - 0.6; launches of small items (Ring with 32 ranks below 4 Mi
+// elements) measured 4 - 12 % slower than on the register kernel.
+constexpr int kNarrowTmaTile = 8192;
+constexpr int64_t kNarrowTmaMinBytes = 8 << 20;
 
-template <hc_dtype_t DT, hc_op_t OP, int MAXI>
+// TILE: bytes per operand per block (kTmaTile, or kNarrowTmaTile)
+template <hc_dtype_t DT, hc_op_t OP, int MAXI, int TILE>
 __global__ void __launch_bounds__(kTmaThreads)
 step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
     constexpr int ES = DT_<DT>::ES;
@@ -247,14 +259,14 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
     const int64_t hi = sbeg + p.hi < send_ ? sbeg + p.hi : send_;
     const int64_t lo = sbeg + p.lo;
     const int64_t nfull = lo < hi ? (hi - lo) / A : 0;
-    const int64_t t0 = tile * kTmaTile;
+    const int64_t t0 = tile * TILE;
     const int acc_slot = I.acc_rank >= 0 ? I.in_cnt : -1;
     const int nops = I.in_cnt + (acc_slot >= 0 ? 1 : 0);
     const bool staged = t0 < nfull * 16;
     const int64_t left = nfull * 16 - t0;
-    const unsigned tb = (unsigned)(left < kTmaTile ? left : kTmaTile);
+    const unsigned tb = (unsigned)(left < TILE ? left : TILE);
     const uintptr_t off = (uintptr_t)lo * ES + (uintptr_t)t0;
-    uint64_t* full = (uint64_t*)(smem + (size_t)nops * kTmaTile);
+    uint64_t* full = (uint64_t*)(smem + (size_t)nops * TILE);
     // Inputs that no launch of this call writes may be requested before the
     // programmatic wait, overlapping the previous launch's tail; everything
     // else (the accumulator, every store) comes after it.
@@ -267,8 +279,8 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
     // mode 0.92 / 0.88 -> 0.95 / 0.93, hierarchical 1.03 -> 1.05)
     const uint64_t first_out = l2_evict_first_policy();
     auto load = [&](int slot, uintptr_t src) {
-        if (I.once) bulk_g2s_hint(smem + (size_t)slot * kTmaTile, src, tb, full, first_out);
-        else bulk_g2s(smem + (size_t)slot * kTmaTile, src, tb, full);
+        if (I.once) bulk_g2s_hint(smem + (size_t)slot * TILE, src, tb, full, first_out);
+        else bulk_g2s(smem + (size_t)slot * TILE, src, tb, full);
     };
     auto issue_inputs = [&]() {
         int r = I.in_rot;
@@ -296,7 +308,6 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
             mbar_expired(full, p.err, p.hold, threadIdx.x == 0);
             return;
         }
-        const unsigned vo = threadIdx.x * 16u;
         if (I.in_cnt == 1 && acc_slot < 0) {
             // a copy: the tile goes from shared memory to every output by
             // bulk stores; the block leaves once they have read it
@@ -308,15 +319,17 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
                 bulk_commit();
                 bulk_wait_read_all();
             }
-        } else if (vo < tb) {
-            uint4 v = *(const uint4*)(smem + vo);
-            for (int j = 1; j < I.in_cnt; j++)
-                v = vop<DT, OP>(v, *(const uint4*)(smem + (size_t)j * kTmaTile + vo));
-            if (acc_slot >= 0) v = vop<DT, OP>(*(const uint4*)(smem + (size_t)acc_slot * kTmaTile + vo), v);
-            const uint64_t last_out = l2_evict_last_policy();
-            each_output(I, [&](int r, bool kept) {
-                st_vec_hint(p.base[I.out_loc][r] + off + vo, v, kept ? last_out : first_out);
-            });
+        } else {
+            for (unsigned vo = threadIdx.x * 16u; vo < tb; vo += kTmaThreads * 16u) {
+                uint4 v = *(const uint4*)(smem + vo);
+                for (int j = 1; j < I.in_cnt; j++)
+                    v = vop<DT, OP>(v, *(const uint4*)(smem + (size_t)j * TILE + vo));
+                if (acc_slot >= 0) v = vop<DT, OP>(*(const uint4*)(smem + (size_t)acc_slot * TILE + vo), v);
+                const uint64_t last_out = l2_evict_last_policy();
+                each_output(I, [&](int r, bool kept) {
+                    st_vec_hint(p.base[I.out_loc][r] + off + vo, v, kept ? last_out : first_out);
+                });
+            }
         }
     }
     if (tile == 0 && threadIdx.x == 0) {
@@ -465,21 +478,21 @@ void* pick_step_op(hc_op_t op) {
     default: return (void*)step_kernel<DT, HC_MIN, MAXI, BATCH>;
     }
 }
-template <int MAXI, hc_dtype_t DT>
+template <int MAXI, int TILE, hc_dtype_t DT>
 void* pick_step_tma_op(hc_op_t op) {
     switch (op) {
-    case HC_SUM: return (void*)step_kernel_tma<DT, HC_SUM, MAXI>;
-    case HC_PROD: return (void*)step_kernel_tma<DT, HC_PROD, MAXI>;
-    case HC_MAX: return (void*)step_kernel_tma<DT, HC_MAX, MAXI>;
-    default: return (void*)step_kernel_tma<DT, HC_MIN, MAXI>;
+    case HC_SUM: return (void*)step_kernel_tma<DT, HC_SUM, MAXI, TILE>;
+    case HC_PROD: return (void*)step_kernel_tma<DT, HC_PROD, MAXI, TILE>;
+    case HC_MAX: return (void*)step_kernel_tma<DT, HC_MAX, MAXI, TILE>;
+    default: return (void*)step_kernel_tma<DT, HC_MIN, MAXI, TILE>;
     }
 }
-template <int MAXI>
+template <int MAXI, int TILE>
 void* pick_step_tma(hc_dtype_t dt, hc_op_t op) {
     switch (dt) {
-    case HC_INT32: return pick_step_tma_op<MAXI, HC_INT32>(op);
-    case HC_FLOAT32: return pick_step_tma_op<MAXI, HC_FLOAT32>(op);
-    default: return pick_step_tma_op<MAXI, HC_BFLOAT16>(op);
+    case HC_INT32: return pick_step_tma_op<MAXI, TILE, HC_INT32>(op);
+    case HC_FLOAT32: return pick_step_tma_op<MAXI, TILE, HC_FLOAT32>(op);
+    default: return pick_step_tma_op<MAXI, TILE, HC_BFLOAT16>(op);
     }
 }
 
@@ -554,16 +567,23 @@ cudaError_t launch_step_items(const Plan& plan, const PlanLaunch& L, size_t firs
     // kernel (the Pipeline AllGather steps before their sends were merged
     // measured 0.89 -> 0.77 on bulk copies).
     bool broadcasts = true;
-    for (const DevItem& it : part.items)
+    int64_t launch_bytes = 0;  // every item's operands and outputs over the slice
+    for (const DevItem& it : part.items) {
         broadcasts = broadcasts && it.in_cnt == 1 && it.acc_rank < 0 && item_outputs(it) >= 3;
-    if ((widest >= 3 || broadcasts) && operands <= kStepTmaMaxOperands && !host_buffers) {
+        launch_bytes += (int64_t)it.seg_width * it.seg_reps * p.vecs * 16 *
+                        (it.in_cnt + (it.acc_rank >= 0 ? 1 : 0) + item_outputs(it));
+    }
+    const bool wide = widest >= 3 || broadcasts;
+    const bool narrow = !wide && launch_bytes >= kNarrowTmaMinBytes;
+    if ((wide || narrow) && operands <= kStepTmaMaxOperands && !host_buffers) {
         // TMA-staged: one block per tile of every segment of every item
-        void* fn = pick_step_tma<MAXI>(dt, op);
+        const int tile = wide ? kTmaTile : kNarrowTmaTile;
+        void* fn = wide ? pick_step_tma<MAXI, kTmaTile>(dt, op) : pick_step_tma<MAXI, kNarrowTmaTile>(dt, op);
         p.err = device_error_flag();
         if (!p.err) return cudaErrorInvalidValue;
-        const int smem = operands * kTmaTile + 16;
+        const int smem = operands * tile + 16;
         if (!allow_smem(fn, smem)) return cudaErrorInvalidValue;
-        p.tiles = std::max<int64_t>(1, (p.vecs * 16 + kTmaTile - 1) / kTmaTile);
+        p.tiles = std::max<int64_t>(1, (p.vecs * 16 + tile - 1) / tile);
         int64_t begin = 0;
         for (DevItem& it : part.items) {
             it.cta_begin = (int32_t)begin;

@@ -331,6 +331,28 @@ def test_tma_staged_paths(algo, dtype):
     assert B.hc_device_status() == 0
 
 
+@pytest.mark.parametrize("algo", ("ring", "rhd"))
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_large_narrow_step_launches(algo, dtype):
+    """Step launches that move 8 MiB or more take the TMA-staged step kernel
+    with 8 KB tiles even when their items are narrow (one input and an
+    accumulator, or a copy): segments ending in a partial tile, a ragged end
+    of the rank vector, RHD's fold and unfold (P = 5), in-place AllReduce,
+    sum and max."""
+    from collective_communication_algorithms_gb300 import _binding as B
+    per_seg = 350003 if dtype != "bfloat16" else 700001
+    for P in (5, 8):
+        n = P * per_seg + 13
+        for op in ("sum", "max"):
+            X = inputs(dtype, P, n, seed=P + 303, op=op)
+            for in_place in (False, True):
+                check("allreduce", algo, X, dtype, op, "step", in_place)
+        X = inputs(dtype, P, n, seed=P + 404, op="sum")
+        check("reducescatter", algo, X, dtype, "sum", "step", False)
+        check("allgather", algo, X, dtype, "sum", "step", False)
+    assert B.hc_device_status() == 0
+
+
 @pytest.mark.parametrize("mode", ["fused", "step"])
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_broadcast(mode, dtype):
