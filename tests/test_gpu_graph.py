@@ -155,3 +155,41 @@ def test_chained_step_calls_read_the_previous_calls_output(use_graph):
     for got, want in ((A, Y1), (Bv, Y2), (C, Y3)):
         assert np.array_equal(got[:, :n].cpu().numpy().view(np.uint32), want.view(np.uint32))
     assert B.hc_device_status() == 0
+
+
+@pytest.mark.parametrize("use_graph", [False, True])
+def test_chained_large_narrow_step_calls(use_graph):
+    """The same for Ring and RHD step calls whose launches move 8 MiB or
+    more and so run on the TMA-staged step kernel with 8 KB tiles, loading
+    the call's own inputs early: Ring, RHD and Ring AllReduces chained on
+    one stream (eagerly, or as one graph), each reading the previous call's
+    output; every result equals the oracle's replay of the chain."""
+    P, n = 8, 8 * 350003 + 13
+    npad = (n + 3) // 4 * 4
+    X = hc_inputs.gradients_f32(P, n, seed=43)
+    dev = torch.zeros((P, npad), dtype=torch.float32, device="cuda")
+    dev[:, :n] = torch.from_numpy(X).cuda()
+    A, Bv, C = torch.zeros_like(dev), torch.zeros_like(dev), torch.zeros_like(dev)
+    step = B.make_opts("step")
+    calls = [(rows(dev), rows(A), "ring"), (rows(A), rows(Bv), "rhd"), (rows(Bv), rows(C), "ring")]
+    stream = torch.cuda.current_stream().cuda_stream
+    torch.cuda.synchronize()
+    if use_graph:
+        g = B.Graph()
+        for s_, r_, algo in calls:
+            g.add_allreduce(s_, r_, P, n, "float32", "sum", algo, step)
+        g.build()
+        assert g.info()["edges"] >= 2
+        g.launch(stream)
+        torch.cuda.synchronize()
+        g.close()
+    else:
+        for s_, r_, algo in calls:
+            B.hc_allreduce(s_, r_, P, n, "float32", "sum", algo, step, stream)
+        torch.cuda.synchronize()
+    Y1 = O.replay("ring", "allreduce", X, "sum", "float32")
+    Y2 = O.replay("rhd", "allreduce", Y1, "sum", "float32")
+    Y3 = O.replay("ring", "allreduce", Y2, "sum", "float32")
+    for got, want in ((A, Y1), (Bv, Y2), (C, Y3)):
+        assert np.array_equal(got[:, :n].cpu().numpy().view(np.uint32), want.view(np.uint32))
+    assert B.hc_device_status() == 0
