@@ -26,6 +26,7 @@ struct FusedParams {
     int owner;                 // Broadcast: the root owns the single segment (-1: segment k's owner is k)
     unsigned long long skip_mask;  // AllGather / Broadcast: ranks whose data is already in place
     unsigned long long wait_ns;    // TMA kernels: limit of the first wait on the copies' mbarrier
+    int prefetch;              // AllGather / Broadcast: 1 = the first S blocks each prefetch one owner's segment into L2
     int* err;                  // device address of the library's error flag (HC_ERR_TIMEOUT on a wait that gave up)
 };
 
@@ -252,6 +253,13 @@ __device__ __forceinline__ uint64_t l2_evict_last_policy() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+// Asynchronous prefetch of [gsrc, gsrc + bytes) into L2 with a cache policy
+// (16-byte aligned address, size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2_hint(uintptr_t gsrc, unsigned bytes, uint64_t policy) {
+    asm volatile("cp.async.bulk.prefetch.L2.global.L2::cache_hint [%0], %1, %2;" ::"l"(gsrc), "r"(bytes),
+                 "l"(policy)
+                 : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

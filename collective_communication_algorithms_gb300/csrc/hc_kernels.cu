@@ -348,6 +348,8 @@ step_kernel_tma(const __grid_constant__ StepParams<MAXI> p) {
     }
 }
 
+constexpr int kAgPrefetchChunk = 32768;  // bytes per L2 prefetch request
+
 // AllGather, register path: segment k read once from its owner, written to
 // every rank (the owner's own copy only when it is not already in place).
 // Broadcast is the same kernel with one segment owned by the root.
@@ -365,6 +367,24 @@ fused_allgather(const __grid_constant__ FusedParams p) {
     const bool skip_own = (p.skip_mask >> k) & 1ull;
     asm volatile("griddepcontrol.wait;" ::: "memory");  // programmatic dependent launch
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (p.prefetch && threadIdx.x == 0) {
+        // the first gridDim.y blocks in launch order each request one owner's
+        // segment into L2 (evict-last, so that the stream of stores does not
+        // push it out before the later blocks read it)
+        const int64_t lin = (int64_t)blockIdx.y * gridDim.x + blockIdx.x;
+        if (lin < gridDim.y) {
+            const int s2 = (int)lin;
+            const int k2 = p.owner >= 0 ? p.owner : s2;
+            const int64_t b2 = (int64_t)s2 * p.L;
+            const int64_t e2 = b2 + p.L < p.n ? b2 + p.L : p.n;
+            const int64_t nb = e2 > b2 ? ((e2 - b2) * ES) / 16 * 16 : 0;
+            const uint64_t keep = l2_evict_last_policy();
+            for (int64_t t = 0; t < nb; t += kAgPrefetchChunk) {
+                const unsigned by = (unsigned)(nb - t < kAgPrefetchChunk ? nb - t : kAgPrefetchChunk);
+                bulk_prefetch_l2_hint(p.src[k2] + (uintptr_t)b2 * ES + (uintptr_t)t, by, keep);
+            }
+        }
+    }
     for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nfull; v += stride) {
         const uintptr_t off = (uintptr_t)(sbeg + v * A) * ES;
         const uint4 x = ld_stream(p.src[k] + off);
@@ -697,6 +717,18 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t stream, int sm_count) 
         // ranks and 1 to 32 Mi elements.  The same store pattern without the
         // loads takes 73.8 us at P = 8, 64 MiB per rank, against 89 - 93 us
         // with them: reads and writes share the DRAM bus.
+        // From 16 ranks, with segments of at most 1 MiB and a source of at
+        // least 8 MiB, the first blocks also prefetch the whole source into
+        // L2 (evict-last).  On GB300 (fp32, out of place, same call): P = 16,
+        // 2 / 4 Mi elements per rank 22.3 -> 21.0 / 42.6 -> 38.7 us; P = 32,
+        // 4 / 8 Mi 83.1 -> 76.2 / 161.6 -> 155.7 us (bf16 8 Mi: 83.1 ->
+        // 76.2); P = 64, 2 / 4 / 8 Mi 84.2 -> 80.5 / 160.8 -> 151.3 / 314 ->
+        // 303 us.  With fewer ranks the segments are long and one thread per
+        // segment cannot issue the requests in time (P = 8, 64 MiB per rank:
+        // 90 -> 131 us); a separate prefetch launch cost 2 us per call and
+        // slowed that case too (93 us); sources under 8 MiB gained nothing
+        // (P = 32, 1 Mi: 22.1 -> 23.0 us).
+        p.prefetch = (a.P >= 16 && seg_bytes <= (1 << 20) && lay.n * es >= (8 << 20) && !a.host_buffers) ? 1 : 0;
         void* fn = es == 2 ? (void*)fused_allgather<2> : (void*)fused_allgather<4>;
         const int64_t vecs = (lay.L + lay.A - 1) / lay.A;
         const int64_t want = std::max<int64_t>(1, (vecs + kFusedThreads - 1) / kFusedThreads);
