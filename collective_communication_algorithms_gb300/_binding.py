@@ -415,8 +415,9 @@ class Graph:
 
 
 def hc_test_expire_waits(enable):
-    """Test hook: TMA-staged fused kernels launched while enabled give up their
-    first shared-memory barrier wait after 1 ms and report HC_ERR_TIMEOUT."""
+    """Test hook: TMA-staged kernels (fused and step) launched while enabled
+    give up their first shared-memory barrier wait after 1 ms and report
+    HC_ERR_TIMEOUT."""
     _check(lib().hc_test_expire_waits(1 if enable else 0), "hc_test_expire_waits")
 
 
