@@ -545,24 +545,29 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
                            hc_dtype_t dtype, hc_mode_t mode, hc_algo_t* out_algo,
                            double* predicted_us) {
     // Constants measured on GB300 (a C caller; bench.py --sweep select, the
-    // benchmark's configurations and a C timing loop around the entry points):
+    // benchmark's configurations and a C timing loop around the entry points),
+    // the device terms fitted to the measured table by least squares on the
+    // log of the time:
     //  host: 0.55 us of the library's own work per call, 1.4 us per launch;
-    //  step mode: the device time per dependent launch of each schedule
-    //    (Ring 1.9 us; RHD 2.2 us below 16 ranks and 2.6 us from 16, whose
-    //    launches carry many items with scattered block sets; Pipeline 2.4 us;
-    //    hierarchical 3.1 us, fewer but heavier launches), and the fraction of
-    //    the copy bandwidth each schedule's steps reach on their own bytes
-    //    (above 1 where the steps' partial sums come back from L2);
-    //  fused mode: a fixed device cost per call that grows with the ranks a
-    //    block reduces (1.55 us + per-rank cost of the schedule's reduction:
-    //    the Ring chain, the RHD tree -- compile-time below 16 ranks, looped
-    //    above --, the Pipeline and hierarchical two-level trees, the
-    //    AllGather's plain copies), then the bytes at the path's fraction of
-    //    the bandwidth (AllReduce / ReduceScatter TMA-staged up to 32 ranks,
-    //    register path above; the AllGather's plain copies, whose writes per
-    //    byte read grow with the ranks).
+    //  step mode: the device time per dependent launch of each schedule (Ring
+    //    1.8 us, RHD 2.0, Pipeline 1.9, hierarchical 2.6 -- fewer but heavier
+    //    launches) plus 0.02 us per rank (the launch's items), and the
+    //    fraction of the copy bandwidth each schedule's steps reach on their
+    //    own bytes (above 1 where a step's outputs come back from L2 as the
+    //    next step's operands);
+    //  fused mode: a fixed device cost per call plus a per-rank cost of the
+    //    schedule's reduction in one block (the Ring chain, the RHD tree --
+    //    compile-time below 16 ranks, looped above --, the Pipeline and
+    //    hierarchical two-level trees, the AllGather's plain copies), then the
+    //    bytes at the path's fraction of the bandwidth (AllReduce /
+    //    ReduceScatter TMA-staged up to 32 ranks, register path above; the
+    //    AllGather, prefetching its source into L2 from 16 ranks);
+    //  both modes: a call whose ranks' vectors fit in L2 (P n b <= 96 MiB)
+    //    moves its bytes 1.44 times faster when its buffers are L2-resident, as
+    //    for calls repeated on the same buffers.
     const double kHostCallUs = 0.55, kHostLaunchUs = 1.4;
-    const double kFusedBaseUs = 1.55, kBandwidth = 6800e9;
+    const double kFusedBaseUs = 1.3, kBandwidth = 6800e9;
+    const double kLaunchPerRankUs = 0.02, kL2HotBytes = 96.0 * (1 << 20), kL2HotFactor = 1.44;
     if (!out_algo || !valid_coll(coll) || !valid_dtype(dtype)) return HC_ERR_INVALID_ARG;
     if (mode != HC_MODE_FUSED && mode != HC_MODE_STEP) return HC_ERR_INVALID_ARG;
     if (P < 1 || P > kMaxRanks) return HC_ERR_INVALID_ARG;
@@ -581,32 +586,35 @@ hc_status_t hc_select_algo(hc_coll_t coll, int P, int ranks_per_server, size_t c
         const int rps = (a == HC_ALGO_PIPELINE || a == HC_ALGO_HIER) ? ranks_per_server : 1;
         if (hc_schedule_stats(a, coll, P, rps, count, dtype, 0, &st, nullptr) != HC_OK) continue;
         double host, dev;
+        const double bw = kBandwidth *
+                          ((double)P * (double)count * elem_bytes(dtype) <= kL2HotBytes ? kL2HotFactor : 1.0);
         if (mode == HC_MODE_STEP) {
-            const double launch_us = a == HC_ALGO_RING       ? 1.9
-                                     : a == HC_ALGO_RHD      ? (P < 16 ? 2.2 : 2.6)
-                                     : a == HC_ALGO_PIPELINE ? 2.4
-                                                             : 3.1;
-            const double f = a == HC_ALGO_RING       ? 1.1
-                             : a == HC_ALGO_RHD      ? 1.0
-                             : a == HC_ALGO_PIPELINE ? 1.1
+            const double launch_us = (a == HC_ALGO_RING       ? 1.8
+                                      : a == HC_ALGO_RHD      ? 2.0
+                                      : a == HC_ALGO_PIPELINE ? 1.9
+                                                              : 2.6) +
+                                     kLaunchPerRankUs * P;
+            const double f = a == HC_ALGO_RING       ? 1.48
+                             : a == HC_ALGO_RHD      ? 1.24
+                             : a == HC_ALGO_PIPELINE ? 1.17
                                                      : 1.12;
             host = kHostCallUs + st.launches_step * kHostLaunchUs;
-            dev = st.launches_step * launch_us + (double)st.step_bytes / (f * kBandwidth) * 1e6;
+            dev = st.launches_step * launch_us + (double)st.step_bytes / (f * bw) * 1e6;
         } else {
             double per_rank, f;
             if (copy) {
-                per_rank = 0.03;
-                f = P < 16 ? 0.94 : 1.02;
+                per_rank = 0.042;
+                f = P < 16 ? 1.05 : 1.09;
             } else {
-                per_rank = a == HC_ALGO_RING       ? 0.055
-                           : a == HC_ALGO_RHD      ? (P < 16 ? 0.04 : 0.067)
-                           : a == HC_ALGO_PIPELINE ? 0.07
-                                                   : 0.083;
-                f = P <= 32 ? 1.0 : 0.96;
+                per_rank = a == HC_ALGO_RING       ? 0.064
+                           : a == HC_ALGO_RHD      ? (P < 16 ? 0.057 : 0.076)
+                           : a == HC_ALGO_PIPELINE ? 0.076
+                                                   : 0.098;
+                f = P <= 32 ? 1.03 : 0.99;
             }
             host = kHostCallUs + st.launches_fused * kHostLaunchUs;
             dev = st.launches_fused ? kFusedBaseUs + per_rank * P +
-                                          (double)st.fused_bytes / (f * kBandwidth) * 1e6
+                                          (double)st.fused_bytes / (f * bw) * 1e6
                                     : 0.0;
         }
         // launches are queued asynchronously: the host cost and the device

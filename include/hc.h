@@ -392,20 +392,23 @@ hc_status_t hc_step_plan(hc_algo_t algo, hc_coll_t coll, int P, int ranks_per_se
  * hides under the memory traffic).  Launches are queued asynchronously, so
  * the host's launch cost and the device time overlap:
  *   t = max(c_host + launches * alpha_host, t_device)
- *   step:  t_device = launches * alpha_algo + step_bytes / (f_algo * B)
+ *   step:  t_device = launches * (alpha_algo + a_rank * P) + step_bytes / (f_algo * B)
  *   fused: t_device = alpha_fused + r_algo * P + fused_bytes / (f_path * B)
  * with launches and bytes from hc_schedule_stats and, measured on GB300 for
- * a C caller: c_host = 0.55 us, alpha_host = 1.4 us per launch; alpha_algo
- * per dependent launch 1.9 us (Ring), 2.2 us (RHD below 16 ranks), 2.6 us
- * (RHD from 16), 2.4 us (Pipeline), 3.1 us (hierarchical); f_algo = 1.1
- * (Ring, Pipeline: their partial sums come back from L2), 1.0 (RHD), 1.12
- * (hierarchical);
- * alpha_fused = 1.55 us, r_algo the per-rank cost of the schedule's
- * reduction in one block (Ring 0.055 us, RHD 0.04 below 16 ranks and 0.067
- * from 16, Pipeline 0.07, hierarchical 0.083, AllGather / Broadcast 0.03),
- * f_path = 1.0 (AllReduce / ReduceScatter up to 32 ranks, 0.96 above), 0.94
- * (AllGather / Broadcast below 16 ranks) or 1.02 (from 16, where each byte
- * read is written more often); B = 6800 GB/s.
+ * a C caller: c_host = 0.55 us, alpha_host = 1.4 us per launch; the device
+ * terms fitted to timed calls of every candidate (36 shapes): alpha_algo per
+ * dependent launch 1.8 us (Ring), 2.0 us (RHD), 1.9 us (Pipeline), 2.6 us
+ * (hierarchical), a_rank = 0.02 us; f_algo = 1.48 (Ring), 1.24 (RHD), 1.17
+ * (Pipeline), 1.12 (hierarchical), above 1 where a step's outputs come back
+ * from L2 as the next step's operands;
+ * alpha_fused = 1.3 us, r_algo the per-rank cost of the schedule's
+ * reduction in one block (Ring 0.064 us, RHD 0.057 below 16 ranks and 0.076
+ * from 16, Pipeline 0.076, hierarchical 0.098, AllGather / Broadcast 0.042),
+ * f_path = 1.03 (AllReduce / ReduceScatter up to 32 ranks, 0.99 above), 1.05
+ * (AllGather / Broadcast below 16 ranks) or 1.09 (from 16, where each byte
+ * read is written more often); B = 6800 GB/s, times 1.44 when the ranks'
+ * vectors fit in L2 (P * count * element size <= 96 MiB: buffers that calls
+ * on the same data keep resident).
  * Candidates: Ring and RHD; Pipeline and, for an AllReduce, the
  * hierarchical AllReduce when ranks_per_server > 1 divides P; Broadcast:
  * RHD only.  Between equal costs the lower device time wins, then the
